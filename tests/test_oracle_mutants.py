@@ -1,0 +1,62 @@
+"""Plant plausible mistakes in copies of the oracle (on the CPU) and require the
+pins to catch every one.  The oracle source is never modified; each mutant is
+compiled from a patched copy in a temporary directory."""
+import os
+
+import pytest
+
+import oracle
+import pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "pkv_oracle.cpp")
+
+# (name, original text, mutated text) — each original must occur exactly once.
+MUTANTS = [
+    ("gqa-interleaved-heads", "const int h = kvh * g + hh;  // query heads",
+     "const int h = hh * Hkv + kvh;  // query heads"),
+    ("gather-wrong-block-index", "const int32_t blk = table_row[j / block_size];",
+     "const int32_t blk = table_row[j % block_size];"),
+    ("gather-offset-off-by-one",
+     "const int64_t slot = static_cast<int64_t>(blk) * block_size + j % block_size;",
+     "const int64_t slot = static_cast<int64_t>(blk) * block_size + (j + 1) % block_size;"),
+    ("causal-off-by-one", "const int64_t n_visible = Lk - Lq + r + 1;",
+     "const int64_t n_visible = Lk - Lq + r;"),
+    ("causal-top-left", "const int64_t n_visible = Lk - Lq + r + 1;",
+     "const int64_t n_visible = r + 1;"),
+    ("no-scale", "s[j] = scale * dot;", "s[j] = dot;"),
+    ("lse-without-max", "*lse = m + std::log(l);", "*lse = std::log(l);"),
+    ("lse-log2", "*lse = m + std::log(l);", "*lse = m + std::log2(l);"),
+    ("no-normalisation", "for (int d = 0; d < D; ++d) out[d] /= l;",
+     "for (int d = 0; d < D; ++d) out[d] /= 1.0;"),
+    ("pv-uses-keys", "const uint16_t* v = &V[static_cast<size_t>(j) * D];",
+     "const uint16_t* v = &K[static_cast<size_t>(j) * D];"),
+    ("gather-swaps-k-v",
+     "std::memcpy(&K[static_cast<size_t>(j) * D], k_cache + src, sizeof(uint16_t) * D);",
+     "std::memcpy(&K[static_cast<size_t>(j) * D], v_cache + src, sizeof(uint16_t) * D);"),
+    ("store-swaps-block-offset", "const int64_t dst = (blk * block_size + off) * row;",
+     "const int64_t dst = (off * num_blocks + blk) * row;"),
+    ("store-k-into-v", "std::memcpy(v_cache + dst, v + t * v_tok_stride, sizeof(uint16_t) * row);",
+     "std::memcpy(v_cache + dst, k + t * k_tok_stride, sizeof(uint16_t) * row);"),
+    ("store-no-duplicate-check", "if (seen[s]) return -3;", "if (false) return -3;"),
+    ("prefill-wrong-q-row", "const int64_t o = row * Hq + h;",
+     "const int64_t o = row * Hq + hh;"),
+    ("softmax-max-not-subtracted-from-weights", "s[j] = std::exp(s[j] - m);",
+     "s[j] = std::exp(s[j]);"),
+]
+
+
+@pytest.mark.parametrize("name,orig,mut", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, orig, mut):
+    src = open(SRC).read()
+    assert src.count(orig) == 1, f"mutation anchor not unique/present: {orig!r}"
+    path = tmp_path / f"mut_{name}.cpp"
+    path.write_text(src.replace(orig, mut))
+    so = oracle.build(str(path), str(tmp_path / f"libmut_{name}.so"))
+    lib = oracle.load(so)
+    failed = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(lib)
+        except (AssertionError, oracle.OracleError) as e:  # caught by this pin
+            failed.append(pin.__name__)
+    assert failed, f"mutant {name} passed every pin"
