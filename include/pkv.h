@@ -1,0 +1,181 @@
+/* pkv.h — C ABI of the paged KV-cache attention library (GB300, sm_103a).
+ *
+ * Three operations make up the data-parallel hot path of attention over a paged
+ * KV cache, as "Nano-vLLM System Architecture Analysis" describes it (§2 Core
+ * Components, "Paged KV Cache" and "Attention with Paged Cache"):
+ *
+ *   kv_cache_store           write new K/V rows into the block pool via slot_mapping
+ *   paged_decode_attention   one query row per (sequence, head) over the whole
+ *                            cached context, read through block_tables
+ *   paged_prefill_attention  causal (chunked) prefill: new query rows over a
+ *                            cached prefix plus the new tokens, all read through
+ *                            block_tables
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or retains them.  Sizes are element counts.
+ *   - Data type: K/V/Q/out are bf16 (IEEE binary16-brain, passed as void*),
+ *     indices are int32, lse is fp32.  Byte offsets are computed in 64 bits.
+ *   - The block pool k_cache / v_cache is one contiguous array per tensor with
+ *     layout [num_blocks, block_size, Hkv, D]; a "slot" is
+ *     block_id * block_size + offset and addresses one [Hkv, D] row.
+ *   - Supported: D == 128, block_size == 256, Hq % Hkv == 0, Hkv >= 1.
+ *     Anything else returns PKV_ERR_SHAPE.
+ *   - Every call is asynchronous on `stream` (0 = legacy default stream), does
+ *     no host synchronisation and no allocation, and returns a status for
+ *     errors it can see on the host.  Errors found by a kernel (a slot or block
+ *     id out of range, a context longer than its block table, a bounded wait
+ *     that ran out) never trap: the kernel skips the bad access, records the
+ *     error in the device error word and finishes; read it with
+ *     pkv_get_device_error().
+ *   - Outputs for rows whose inputs were invalid are unspecified.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pkv_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_ARG = -1,          /* null pointer, negative size, misaligned pointer  */
+  PKV_ERR_SHAPE = -2,        /* unsupported D / block_size / head counts          */
+  PKV_ERR_WORKSPACE = -3,    /* workspace missing, too small or misaligned        */
+  PKV_ERR_LAUNCH = -4,       /* a CUDA runtime call or kernel launch failed       */
+  PKV_ERR_DEVICE_INDEX = -5, /* device: slot/block id out of range, ctx > table   */
+  PKV_ERR_TIMEOUT = -6       /* device: a bounded wait ran out                    */
+} pkv_status;
+
+/* kv_cache_store — "Stores computed K/V entries into the paged cache via
+ * slot_mapping" (Nano-vLLM System Architecture Analysis, §2 Core Components,
+ * "Attention with Paged Cache"; blocks of 256 tokens per "Paged KV Cache").
+ *
+ * For every token t in [0, T) with s = slot_mapping[t]:
+ *   s <  0                        : padding, nothing is written;
+ *   0 <= s < num_blocks*block_size: k_cache[s, :, :] = k[t, :, :] and
+ *                                   v_cache[s, :, :] = v[t, :, :] (bit copy);
+ *   s >= num_blocks*block_size    : skipped, device error PKV_ERR_DEVICE_INDEX.
+ * k, v         : bf16 rows [T, Hkv, D]; row t starts at k + t*k_tok_stride
+ *                elements (the [Hkv, D] part of a row is contiguous).  Rows
+ *                whose start is 16-byte aligned are moved in 16-byte vectors,
+ *                others element by element.
+ * k_cache/v_cache : pool [num_blocks, block_size, Hkv, D], 16-byte aligned.
+ * slot_mapping : int32 [T] on the device.
+ * Two tokens with the same non-negative slot: which one lands is unspecified.
+ * Returns PKV_OK, PKV_ERR_ARG (null pointer with T > 0, T < 0, stride smaller
+ * than Hkv*D, misaligned pool), PKV_ERR_SHAPE or PKV_ERR_LAUNCH.  T == 0 is a
+ * no-op. */
+int kv_cache_store(const void* k, const void* v, int64_t k_tok_stride,
+                   int64_t v_tok_stride, void* k_cache, void* v_cache,
+                   const int32_t* slot_mapping, int64_t T, int Hkv, int D,
+                   int block_size, int64_t num_blocks, pkv_stream_t stream);
+
+/* paged_decode_workspace_bytes — bytes of device workspace that a
+ * paged_decode_attention call with the same (B, Hq, Hkv, D, max_blocks_per_seq,
+ * block_size, num_splits) needs.  0 means the call needs none (a single split).
+ * Returns 0 as well for arguments the decode call would reject. */
+size_t paged_decode_workspace_bytes(int B, int Hq, int Hkv, int D,
+                                    int max_blocks_per_seq, int block_size,
+                                    int num_splits);
+
+/* paged_decode_num_splits — the number of context splits a decode call with
+ * these arguments uses (num_splits == 0 picks it from the SM count of the
+ * current device).  Returns a value >= 1, or a negative pkv_status. */
+int paged_decode_num_splits(int B, int Hq, int Hkv, int D, int max_blocks_per_seq,
+                            int block_size, int num_splits);
+
+/* paged_decode_attention — decode attention over the paged cache: "During
+ * decode, gathers all cached K/V from paged blocks before calling
+ * scaled_dot_product_attention" (Nano-vLLM System Architecture Analysis, §2
+ * Core Components, "Attention with Paged Cache"); GQA per §6 "Architecture
+ * Support".  The library reads the blocks in place instead of gathering them.
+ *
+ * For sequence b with L = context_lens[b] (the token stored this step
+ * included) and query head h, with kv head kh = h / (Hq/Hkv):
+ *   key/value j (0 <= j < L) is row kh of slot
+ *       block_tables[b*max_blocks_per_seq + j/block_size]*block_size + j%block_size,
+ *   s_j  = scale * <q[b,h,:], K_j>,
+ *   out[b,h,:] = sum_j softmax(s)_j * V_j       (bf16, round to nearest even),
+ *   lse[b,h]   = ln(sum_j exp(s_j))             (fp32; may be NULL).
+ * L == 0 gives out = 0 and lse = -inf.  No mask: the query is the last
+ * position of its sequence.
+ * q   : bf16 [B, Hq, D] contiguous.   out : bf16 [B, Hq, D] contiguous.
+ * block_tables : int32 [B, max_blocks_per_seq]; only entries < ceil(L/bs) are
+ *                read.  context_lens : int32 [B].  Both on the device.
+ * Accumulation is fp32.  The context is cut into num_splits ranges of whole
+ * blocks (0 = automatic; a requested count is raised when a range would
+ * exceed 32 blocks, and paged_decode_num_splits() reports the count used);
+ * each range is reduced by its own thread block, and the last one to finish
+ * merges the partial results by log-sum-exp.
+ * workspace : device memory of at least paged_decode_workspace_bytes(...)
+ *   bytes, 256-byte aligned; may be NULL when that size is 0.  Its first
+ *   1 MiB holds one arrival counter per (sequence, kv head group), at the same
+ *   place for every call shape; the rest holds the partial results.  That
+ *   first MiB must be zero before the first call that uses a given workspace
+ *   (e.g. cudaMemsetAsync once after allocating it); every call leaves it zero
+ *   again, so one workspace can serve calls of any shape.  Calls that share a
+ *   workspace must not overlap in time (same stream, or ordered by events).
+ * Returns PKV_OK, PKV_ERR_ARG, PKV_ERR_SHAPE, PKV_ERR_WORKSPACE or
+ * PKV_ERR_LAUNCH.  A context longer than max_blocks_per_seq*block_size or a
+ * block id outside [0, num_blocks) is reported as PKV_ERR_DEVICE_INDEX through
+ * pkv_get_device_error() (that read is clamped or skipped, never performed). */
+int paged_decode_attention(void* out, float* lse, const void* q,
+                           const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* context_lens, int B, int Hq, int Hkv,
+                           int D, int block_size, int64_t num_blocks, float scale,
+                           void* workspace, size_t workspace_bytes,
+                           int num_splits, pkv_stream_t stream);
+
+/* paged_prefill_attention — causal prefill / chunked prefill with a prefix
+ * cache: "During prefill with prefix cache, gathers cached K/V from the paged
+ * cache and concatenates with newly computed ones" (Nano-vLLM System
+ * Architecture Analysis, §2 Core Components, "Attention with Paged Cache");
+ * chunked prefill per §2 "Scheduler".
+ *
+ * Sequence i has Lq = cu_seqlens_q[i+1]-cu_seqlens_q[i] new query rows and
+ * Lk = cu_seqlens_k[i+1]-cu_seqlens_k[i] keys: its cached prefix (Lk-Lq tokens)
+ * followed by the Lq new tokens.  The new tokens' K/V must already be in the
+ * pool (kv_cache_store first): every key is read through block_tables, so the
+ * "concatenation" is the block table itself.  Query row r (0 <= r < Lq) of
+ * sequence i and head h sees keys j <= Lk - Lq + r (bottom-right causal):
+ *   out[cu_seqlens_q[i]+r, h, :] = sum_j softmax(s)_j V_j,  s_j = scale <q, K_j>,
+ *   lse[cu_seqlens_q[i]+r, h]    = ln(sum_j exp(s_j))  (may be NULL).
+ * q   : bf16 [sum Lq, Hq, D] contiguous.   out : bf16 [sum Lq, Hq, D].
+ * cu_seqlens_q / cu_seqlens_k : int32 [B+1], device.  max_seqlen_q bounds every
+ * Lq (it sizes the grid) and max_seqlen_k every Lk.
+ * QK^T and PV run on the tcgen05 tensor cores with bf16 operands and fp32
+ * accumulation in tensor memory; the probabilities P are rounded to bf16 for
+ * the PV product.
+ * Returns PKV_OK, PKV_ERR_ARG (null pointers, negative sizes), PKV_ERR_SHAPE or
+ * PKV_ERR_LAUNCH.  Lk < Lq, Lq > max_seqlen_q or Lk > max_seqlen_k, and
+ * out-of-range block ids, are reported as PKV_ERR_DEVICE_INDEX through
+ * pkv_get_device_error() and those rows are left unwritten. */
+int paged_prefill_attention(void* out, float* lse, const void* q,
+                            const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                            int B, int max_seqlen_q, int max_seqlen_k, int Hq,
+                            int Hkv, int D, int block_size, int64_t num_blocks,
+                            float scale, pkv_stream_t stream);
+
+/* pkv_get_device_error — synchronises `stream`, then reads and clears the
+ * device error word of the current device.  Returns PKV_OK, the first error
+ * class recorded (PKV_ERR_DEVICE_INDEX before PKV_ERR_TIMEOUT), or
+ * PKV_ERR_LAUNCH if the synchronisation itself failed. */
+int pkv_get_device_error(pkv_stream_t stream);
+
+/* pkv_status_string — static, human-readable name of a status code. */
+const char* pkv_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,227 @@
+// api.cu — the C ABI entry points declared in include/pkv.h: argument checks,
+// per-device state (SM count, the device error word), TMA tensor-map encoding
+// and dispatch to the kernels.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// The one piece of state the library keeps: a sticky error word per device,
+// or-ed by kernels and read-and-cleared by pkv_get_device_error().
+__device__ unsigned g_device_error;
+
+std::mutex g_mu;
+int g_sm_count[kMaxDevices];
+unsigned* g_err_ptr[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+int device_sm_count() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+unsigned* device_error_word() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+bool encode_pool_map(CUtensorMap* map, const void* base, int64_t num_slots, int Hkv,
+                     int box_rows) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return false;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  // [slots, Hkv, D] with D innermost; a box is 64 dims (128 B, the swizzle
+  // span) x 1 head x box_rows consecutive slots.
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(Hkv),
+                              static_cast<cuuint64_t>(num_slots)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
+                                 static_cast<cuuint64_t>(Hkv) * kHeadDim * 2};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+int check_pool(int Hkv, int D, int block_size, int64_t num_blocks) {
+  if (Hkv <= 0 || D <= 0 || block_size <= 0 || num_blocks < 0) return PKV_ERR_ARG;
+  if (D != kHeadDim || block_size != kBlockSize) return PKV_ERR_SHAPE;
+  // TMA coordinates are 32-bit: every slot index must fit.
+  if (num_blocks * kBlockSize > INT32_MAX) return PKV_ERR_SHAPE;
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" int kv_cache_store(const void* k, const void* v, int64_t k_tok_stride,
+                              int64_t v_tok_stride, void* k_cache, void* v_cache,
+                              const int32_t* slot_mapping, int64_t T, int Hkv, int D,
+                              int block_size, int64_t num_blocks, pkv_stream_t stream) {
+  if (T < 0) return PKV_ERR_ARG;
+  int st = check_pool(Hkv, D, block_size, num_blocks);
+  if (st) return st;
+  if (T == 0) return PKV_OK;
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_ARG;
+  const int64_t row = static_cast<int64_t>(Hkv) * D;
+  if (k_tok_stride < row || v_tok_stride < row) return PKV_ERR_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ARG;
+  unsigned* err = device_error_word();
+  if (!err) return PKV_ERR_LAUNCH;
+  StoreArgs a{k, v, k_tok_stride, v_tok_stride, k_cache, v_cache, slot_mapping, T,
+              static_cast<int>(row), num_blocks * block_size};
+  return launch_store(a, err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t paged_decode_workspace_bytes(int B, int Hq, int Hkv, int D,
+                                               int max_blocks_per_seq, int block_size,
+                                               int num_splits) {
+  if (D != kHeadDim || block_size != kBlockSize || num_splits < 0) return 0;
+  DecodePlan plan;
+  if (plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), &plan))
+    return 0;
+  return plan.workspace_bytes;
+}
+
+extern "C" int paged_decode_num_splits(int B, int Hq, int Hkv, int D, int max_blocks_per_seq,
+                                       int block_size, int num_splits) {
+  if (D != kHeadDim || block_size != kBlockSize) return PKV_ERR_SHAPE;
+  if (num_splits < 0) return PKV_ERR_ARG;
+  DecodePlan plan;
+  const int st = plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), &plan);
+  return st ? st : plan.num_splits;
+}
+
+extern "C" int paged_decode_attention(void* out, float* lse, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_tables,
+                                      int max_blocks_per_seq, const int32_t* context_lens, int B,
+                                      int Hq, int Hkv, int D, int block_size, int64_t num_blocks,
+                                      float scale, void* workspace, size_t workspace_bytes,
+                                      int num_splits, pkv_stream_t stream) {
+  if (B < 0 || Hq <= 0 || max_blocks_per_seq < 0 || num_splits < 0) return PKV_ERR_ARG;
+  int st = check_pool(Hkv, D, block_size, num_blocks);
+  if (st) return st;
+  if (Hq % Hkv) return PKV_ERR_SHAPE;
+  if (B == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !context_lens) return PKV_ERR_ARG;
+  if (max_blocks_per_seq > 0 && !block_tables) return PKV_ERR_ARG;
+  if (num_blocks == 0 && max_blocks_per_seq > 0) return PKV_ERR_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_ARG;
+  DecodePlan plan;
+  st = plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), &plan);
+  if (st) return st;
+  if (plan.workspace_bytes) {
+    if (!workspace || workspace_bytes < plan.workspace_bytes ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+      return PKV_ERR_WORKSPACE;
+  }
+  unsigned* err = device_error_word();
+  if (!err) return PKV_ERR_LAUNCH;
+  DecodeArgs a{out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+               B, Hq, Hkv, num_blocks, scale, workspace, workspace_bytes, num_splits};
+  return launch_decode(a, plan, err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int paged_prefill_attention(void* out, float* lse, const void* q, const void* k_cache,
+                                       const void* v_cache, const int32_t* block_tables,
+                                       int max_blocks_per_seq, const int32_t* cu_seqlens_q,
+                                       const int32_t* cu_seqlens_k, int B, int max_seqlen_q,
+                                       int max_seqlen_k, int Hq, int Hkv, int D, int block_size,
+                                       int64_t num_blocks, float scale, pkv_stream_t stream) {
+  if (B < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || Hq <= 0 || max_blocks_per_seq < 0)
+    return PKV_ERR_ARG;
+  int st = check_pool(Hkv, D, block_size, num_blocks);
+  if (st) return st;
+  if (Hq % Hkv) return PKV_ERR_SHAPE;
+  if (B == 0 || max_seqlen_q == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k) return PKV_ERR_ARG;
+  if (max_blocks_per_seq > 0 && !block_tables) return PKV_ERR_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_ARG;
+  if (static_cast<int64_t>(max_seqlen_k) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
+    return PKV_ERR_ARG;
+  unsigned* err = device_error_word();
+  if (!err) return PKV_ERR_LAUNCH;
+  PrefillArgs a{out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, cu_seqlens_q,
+                cu_seqlens_k, B, max_seqlen_q, max_seqlen_k, Hq, Hkv, num_blocks, scale};
+  return launch_prefill(a, err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int pkv_get_device_error(pkv_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PKV_ERR_LAUNCH;
+  unsigned* p = device_error_word();
+  if (!p) return PKV_ERR_LAUNCH;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return PKV_ERR_LAUNCH;
+  if (v) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+      return PKV_ERR_LAUNCH;
+  }
+  if (v & kErrIndex) return PKV_ERR_DEVICE_INDEX;
+  if (v & kErrTimeout) return PKV_ERR_TIMEOUT;
+  return PKV_OK;
+}
+
+extern "C" const char* pkv_status_string(int status) {
+  switch (status) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_ARG: return "PKV_ERR_ARG: invalid argument";
+    case PKV_ERR_SHAPE: return "PKV_ERR_SHAPE: unsupported shape";
+    case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE: workspace missing, small or misaligned";
+    case PKV_ERR_LAUNCH: return "PKV_ERR_LAUNCH: CUDA runtime or launch failure";
+    case PKV_ERR_DEVICE_INDEX: return "PKV_ERR_DEVICE_INDEX: index out of range on the device";
+    case PKV_ERR_TIMEOUT: return "PKV_ERR_TIMEOUT: a device wait ran out";
+    default: return "unknown pkv status";
+  }
+}

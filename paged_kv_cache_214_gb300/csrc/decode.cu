@@ -1,0 +1,530 @@
+// decode.cu — paged decode attention (split-K flash-decoding) for sm_103a.
+//
+// Operation: "During decode, gathers all cached K/V from paged blocks before
+// calling scaled_dot_product_attention" (Nano-vLLM System Architecture
+// Analysis, §2 Core Components, "Attention with Paged Cache"), GQA per §6.
+// Decode is the memory-bound phase (same page, "Differences", §3 "Prefill vs.
+// Decode Separation"), so this kernel never materialises the gathered K/V: it
+// streams each sequence's blocks straight from the pool once.
+//
+// Work decomposition
+//   grid = (S splits, Hkv * head_groups, B).  One thread block owns one
+//   (sequence, kv head, range of whole KV blocks) and serves the G query heads
+//   of that kv head's group that it is assigned, so each K/V byte is read from
+//   HBM once per G heads.
+//   Warp 4 (producer): lane 0 streams the range's K and V through a 3-stage
+//   ring of shared-memory tiles with TMA (64 tokens x 128 dims per tile; two
+//   64-dim boxes per operand, 128-byte swizzle) and mbarrier completion.
+//   Warps 0-3 (consumers): sixteen 8-lane groups, each an independent online
+//   softmax stream.  Lane j of a group owns dims [8j, 8j+8) and [64+8j, 64+8j+8)
+//   of q and of the running output for all G heads, all in registers.  A group
+//   takes one token row per step: 16 partial products per head, a 3-level
+//   butterfly to finish the dot product, then the running max / sum update and
+//   o += p * v on the same 16 dims.
+//   End of the range: the 16 streams are merged by log-sum-exp (shuffles
+//   across the groups of a warp, then shared memory across warps).
+//   With one split the block writes out/lse directly.  Otherwise it writes a
+//   normalised partial (o, log2-sum-exp) to the workspace and takes a ticket
+//   from the (sequence, head group) counter; the last block to arrive merges all
+//   partials with a warp-shuffle log-sum-exp reduction, writes out/lse and
+//   resets the counter, so nothing ever spins.
+// Scores are kept in base-2 units (q is pre-scaled by scale*log2(e)) and
+// converted to a natural-log LSE on output.
+
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kTile = 64;                       // tokens per pipeline stage
+constexpr int kStages = 3;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kHalfBytes = kTile * 128;         // 64 rows x 64 dims x 2 B
+constexpr int kOperandBytes = 2 * kHalfBytes;   // one of K or V for a tile
+constexpr int kStageBytes = 2 * kOperandBytes;  // K and V
+constexpr int kMaxSplitBlocks = 32;             // block ids prefetched per split
+constexpr int kMaxSplits = 1024;
+// Arrival counters live in a fixed region at the start of the workspace, the
+// same for every call shape, so partial results of one call can never land
+// where another call keeps its counters.
+constexpr size_t kCounterRegion = size_t(1) << 20;
+constexpr int64_t kMaxCounters = kCounterRegion / sizeof(unsigned);
+constexpr float kLn2 = 0.69314718055994530942f;
+
+struct DecodeParams {
+  __nv_bfloat16* out;
+  float* lse;
+  const __nv_bfloat16* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float* ws_o;        // [B*Hq, S, 128] normalised partial outputs
+  float* ws_lse;      // [B*Hq, S] partial log2-sum-exp
+  unsigned* ws_count; // [B * Hkv * head_groups] arrival counters
+  unsigned* err;
+  int B, Hq, Hkv, maxblk, num_splits, split_blocks, head_groups;
+  int64_t num_blocks;
+  float scale_log2;
+};
+
+template <int G>
+struct SmemLayout {
+  static constexpr int kMergeO = kStages * kStageBytes;                      // [4][G][128] f32
+  static constexpr int kMergeM = kMergeO + kConsumerWarps * G * 128 * 4;     // [4][G]
+  static constexpr int kMergeL = kMergeM + kConsumerWarps * G * 4;           // [4][G]
+  static constexpr int kBlk = kMergeL + kConsumerWarps * G * 4;              // [32] int
+  static constexpr int kBars = kBlk + kMaxSplitBlocks * 4;                   // full[], empty[]
+  static constexpr int kFlags = kBars + 2 * kStages * 8;                     // abort, last, issued
+  static constexpr int kEnd = kFlags + 16;
+  static constexpr int kBytes = kEnd + 1024;                                 // + alignment slack
+};
+
+__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
+  f[0] = bf16lo(u.x); f[1] = bf16hi(u.x);
+  f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
+  f[4] = bf16lo(u.z); f[5] = bf16hi(u.z);
+  f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
+}
+
+// Weight of a stream with log2-max m against the common max mn (0 for an
+// empty stream).
+__device__ __forceinline__ float rescale(float m, float mn) {
+  return m == -INFINITY ? 0.f : ex2(m - mn);
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 2)
+paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
+                    const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
+  using L = SmemLayout<G>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* merge_o = reinterpret_cast<float*>(smem + L::kMergeO);
+  float* merge_m = reinterpret_cast<float*>(smem + L::kMergeM);
+  float* merge_l = reinterpret_cast<float*>(smem + L::kMergeL);
+  int* sblk = reinterpret_cast<int*>(smem + L::kBlk);
+  volatile int* flags = reinterpret_cast<volatile int*>(smem + L::kFlags);
+  const uint32_t bars = smem_addr(smem + L::kBars);
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
+
+  const int split = blockIdx.x;
+  const int hg = blockIdx.y;  // kv head * head_groups + head group
+  const int b = blockIdx.z;
+  const int kvh = hg / p.head_groups;
+  const int h0 = kvh * (p.Hq / p.Hkv) + (hg % p.head_groups) * G;  // first query head
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  // Context of this sequence (clamped to what its block table can address).
+  int ctx = p.context_lens[b];
+  const int cap = p.maxblk * kBlockSize;
+  if (ctx < 0 || ctx > cap) {
+    if (tid == 0 && split == 0 && hg == 0) record_error(p.err, kErrIndex);
+    ctx = ctx < 0 ? 0 : cap;
+  }
+  const int split_tokens = p.split_blocks * kBlockSize;
+  const int nsplit = (ctx + split_tokens - 1) / split_tokens;
+  if (split >= (nsplit > 0 ? nsplit : 1)) return;  // whole block exits: no work
+
+  if (ctx == 0) {  // empty context: out = 0, lse = -inf
+    for (int i = tid; i < G * kHeadDim; i += kThreads) {
+      const int h = i / kHeadDim, d = i % kHeadDim;
+      p.out[(static_cast<int64_t>(b) * p.Hq + h0 + h) * kHeadDim + d] = __float2bfloat16_rn(0.f);
+    }
+    if (p.lse && tid < G) p.lse[static_cast<int64_t>(b) * p.Hq + h0 + tid] = -INFINITY;
+    return;
+  }
+
+  const int tok_begin = split * split_tokens;
+  const int tok_end = min(ctx, tok_begin + split_tokens);
+  const int n_tiles = (tok_end - tok_begin + kTile - 1) / kTile;
+  const int blk_begin = split * p.split_blocks;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), kConsumerWarps);
+    }
+    flags[0] = 0;  // abort
+    flags[1] = 0;  // last-arrival flag
+    flags[2] = 0;  // tiles issued
+    fence_barrier_init();
+  }
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      tma_prefetch_map(&kmap);
+      tma_prefetch_map(&vmap);
+    }
+    // Block ids of this range (validated; a bad id is reported and replaced by
+    // block 0 so that no out-of-range address is ever formed).
+    const int nblk = (tok_end - 1) / kBlockSize - blk_begin + 1;
+    if (lane < nblk) {
+      int id = p.block_tables[static_cast<int64_t>(b) * p.maxblk + blk_begin + lane];
+      if (id < 0 || id >= p.num_blocks) {
+        record_error(p.err, kErrIndex);
+        id = 0;
+      }
+      sblk[lane] = id;
+    }
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t policy = l2_policy_evict_first();
+      int it = 0;
+      for (; it < n_tiles; ++it) {
+        const int s = it % kStages;
+        if (it >= kStages && !mbar_wait(empty_bar(s), ((it / kStages) - 1) & 1)) {
+          record_error(p.err, kErrTimeout);
+          flags[0] = 1;
+          break;
+        }
+        if (flags[0]) break;
+        const int tok = tok_begin + it * kTile;
+        const int slot = sblk[tok / kBlockSize - blk_begin] * kBlockSize + tok % kBlockSize;
+        const uint32_t kdst = smem_addr(smem + s * kStageBytes);
+        const uint32_t vdst = kdst + kOperandBytes;
+        mbar_arrive_expect_tx(full_bar(s), kStageBytes);
+        tma_load_3d_hint(kdst, &kmap, full_bar(s), 0, kvh, slot, policy);
+        tma_load_3d_hint(kdst + kHalfBytes, &kmap, full_bar(s), 64, kvh, slot, policy);
+        tma_load_3d_hint(vdst, &vmap, full_bar(s), 0, kvh, slot, policy);
+        tma_load_3d_hint(vdst + kHalfBytes, &vmap, full_bar(s), 64, kvh, slot, policy);
+      }
+      flags[2] = it;
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int grp = lane >> 3;  // group within the warp
+    const int j = lane & 7;     // lane within the group: dims [8j,8j+8) and [64+8j,64+8j+8)
+    float qf[G][16];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const __nv_bfloat16* qp = p.q + (static_cast<int64_t>(b) * p.Hq + h0 + h) * kHeadDim;
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(qp + 8 * j));
+      const uint4 c = __ldg(reinterpret_cast<const uint4*>(qp + 64 + 8 * j));
+      unpack8(a, &qf[h][0]);
+      unpack8(c, &qf[h][8]);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) qf[h][i] *= p.scale_log2;
+    }
+    float o[G][16];
+    float m[G], l[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) o[h][i] = 0.f;
+    }
+
+    for (int it = 0; it < n_tiles; ++it) {
+      const int s = it % kStages;
+      if (flags[0]) break;
+      if (!mbar_wait(full_bar(s), (it / kStages) & 1)) {
+        record_error(p.err, kErrTimeout);
+        flags[0] = 1;
+        break;
+      }
+      const int n_valid = min(kTile, tok_end - (tok_begin + it * kTile));
+      const uint32_t kb = smem_addr(smem + s * kStageBytes);
+      const uint32_t vb = kb + kOperandBytes;
+
+      float sc[4][G];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int t = 16 * r + 4 * warp + grp;
+        const uint32_t off = t * 128 + ((j ^ (t & 7)) << 4);
+        float kf[16];
+        unpack8(lds128(kb + off), &kf[0]);
+        unpack8(lds128(kb + kHalfBytes + off), &kf[8]);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            a0 = fmaf(qf[h][i], kf[i], a0);
+            a1 = fmaf(qf[h][8 + i], kf[8 + i], a1);
+          }
+          float acc = a0 + a1;
+          acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+          acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+          acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+          sc[r][h] = t < n_valid ? acc : -INFINITY;
+        }
+      }
+      // online softmax update, once per tile
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float mt = fmaxf(fmaxf(sc[0][h], sc[1][h]), fmaxf(sc[2][h], sc[3][h]));
+        const float mn = fmaxf(m[h], mt);
+        if (mn != -INFINITY) {
+          const float alpha = rescale(m[h], mn);
+          l[h] *= alpha;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[h][i] *= alpha;
+          m[h] = mn;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            sc[r][h] = ex2(sc[r][h] - mn);  // -inf -> 0
+            l[h] += sc[r][h];
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int t = 16 * r + 4 * warp + grp;
+        if (t < n_valid) {
+          const uint32_t off = t * 128 + ((j ^ (t & 7)) << 4);
+          float vf[16];
+          unpack8(lds128(vb + off), &vf[0]);
+          unpack8(lds128(vb + kHalfBytes + off), &vf[8]);
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[h][i] = fmaf(sc[r][h], vf[i], o[h][i]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(s));
+    }
+
+    // merge the four groups of this warp (lanes j, j+8, j+16, j+24)
+#pragma unroll
+    for (int sh = 8; sh <= 16; sh <<= 1) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m[h], sh);
+        const float lo = __shfl_xor_sync(0xffffffffu, l[h], sh);
+        const float mn = fmaxf(m[h], mo);
+        const float a = rescale(m[h], mn), c = rescale(mo, mn);
+        l[h] = l[h] * a + lo * c;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          o[h][i] = o[h][i] * a + __shfl_xor_sync(0xffffffffu, o[h][i], sh) * c;
+        m[h] = mn;
+      }
+    }
+    if (grp == 0) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float* dst = merge_o + (warp * G + h) * kHeadDim;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          dst[8 * j + i] = o[h][i];
+          dst[64 + 8 * j + i] = o[h][8 + i];
+        }
+        if (j == 0) {
+          merge_m[warp * G + h] = m[h];
+          merge_l[warp * G + h] = l[h];
+        }
+      }
+    }
+  }
+
+  __syncthreads();
+  // After a timeout, wait (bounded) for copies still in flight before the
+  // block's shared memory can be released.
+  if (flags[0] && tid == 0) {
+    const int issued = flags[2];
+    for (int s = 0; s < kStages; ++s) {
+      int last = -1;
+      for (int it = s; it < issued; it += kStages) last = it;
+      if (last >= 0) (void)mbar_wait(full_bar(s), (last / kStages) & 1);
+    }
+  }
+  if (warp == kConsumerWarps) return;
+
+  // ---------------------------------------------------------------- epilogue
+  // thread tid (0..127) owns dim d = tid of every head
+  const int d = tid;
+  const bool single = nsplit == 1;
+  for (int h = 0; h < G; ++h) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge_m[w * G + h]);
+    float Ls = 0.f, Os = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float c = rescale(merge_m[w * G + h], M);
+      Ls += merge_l[w * G + h] * c;
+      Os += merge_o[(w * G + h) * kHeadDim + d] * c;
+    }
+    const float on = Os / Ls;
+    const float lse2 = M + __log2f(Ls);
+    const int64_t row = static_cast<int64_t>(b) * p.Hq + h0 + h;
+    if (single) {
+      p.out[row * kHeadDim + d] = __float2bfloat16_rn(on);
+      if (p.lse && d == 0) p.lse[row] = lse2 * kLn2;
+    } else {
+      const int64_t prow = row * p.num_splits + split;
+      __stcg(p.ws_o + prow * kHeadDim + d, on);
+      if (d == 0) __stcg(p.ws_lse + prow, lse2);
+    }
+  }
+  if (single) return;
+
+  // ---------------------------------------------------------------- split merge
+  __threadfence();
+  named_barrier(1, kConsumerWarps * 32);
+  unsigned* counter = p.ws_count + static_cast<int64_t>(b) * p.Hkv * p.head_groups + hg;
+  if (tid == 0) {
+    const unsigned ticket = atomicAdd(counter, 1u);
+    flags[1] = (ticket == static_cast<unsigned>(nsplit - 1)) ? 1 : 0;
+  }
+  named_barrier(1, kConsumerWarps * 32);
+  if (!flags[1]) return;
+  __threadfence();
+  for (int h = warp; h < G; h += kConsumerWarps) {
+    const int64_t row = static_cast<int64_t>(b) * p.Hq + h0 + h;
+    const float* lrow = p.ws_lse + row * p.num_splits;
+    // lanes over splits: max and sum of 2^(lse_s - max) by warp shuffles
+    float mx = -INFINITY;
+    for (int s = lane; s < nsplit; s += 32) mx = fmaxf(mx, __ldcg(lrow + s));
+#pragma unroll
+    for (int sh = 16; sh >= 1; sh >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
+    float sum = 0.f;
+    for (int s = lane; s < nsplit; s += 32) sum += rescale(__ldcg(lrow + s), mx);
+#pragma unroll
+    for (int sh = 16; sh >= 1; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
+    const float inv = 1.f / sum;
+    // lanes over dims (4 each): out = sum_s w_s * o_s
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < nsplit; ++s) {
+      const float w = rescale(__ldcg(lrow + s), mx) * inv;
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(
+          p.ws_o + (row * p.num_splits + s) * kHeadDim) + lane);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+    __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 packed;
+    packed.x = *reinterpret_cast<uint32_t*>(&lo2);
+    packed.y = *reinterpret_cast<uint32_t*>(&hi2);
+    *reinterpret_cast<uint2*>(p.out + row * kHeadDim + 4 * lane) = packed;
+    if (p.lse && lane == 0) p.lse[row] = (mx + __log2f(sum)) * kLn2;
+  }
+  if (tid == 0) *counter = 0u;  // ready for the next call
+}
+
+template <int G>
+int launch_g(const DecodeArgs& a, const DecodePlan& plan, const DecodeParams& prm,
+             const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t stream) {
+  using L = SmemLayout<G>;
+  static_assert(L::kBytes <= 113 * 1024, "two blocks per SM must fit");
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(paged_decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::kBytes) != cudaSuccess)
+      return PKV_ERR_LAUNCH;
+    attr_set[dev] = true;
+  }
+  dim3 grid(plan.num_splits, a.Hkv * plan.head_groups, a.B);
+  paged_decode_kernel<G><<<grid, kThreads, L::kBytes, stream>>>(km, vm, prm);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+int plan_decode(int B, int Hq, int Hkv, int max_blocks_per_seq, int num_splits,
+                int sm_count, DecodePlan* plan) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || max_blocks_per_seq < 0) return PKV_ERR_ARG;
+  if (Hq % Hkv) return PKV_ERR_SHAPE;
+  const int g = Hq / Hkv;
+  const int G = (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1;
+  plan->heads_per_cta = G;
+  plan->head_groups = g / G;
+  const int maxblk = max_blocks_per_seq > 0 ? max_blocks_per_seq : 1;
+  int split_blocks;
+  if (num_splits > 0) {
+    split_blocks = (maxblk + num_splits - 1) / num_splits;
+  } else {
+    // Enough (sequence, head group, split) units for about eight waves of two
+    // blocks per SM if every context were full length; whole blocks per split.
+    const int64_t units = static_cast<int64_t>(B) * Hkv * plan->head_groups * maxblk;
+    const int64_t target = static_cast<int64_t>(sm_count > 0 ? sm_count : 148) * 2 * 8;
+    split_blocks = static_cast<int>((units + target - 1) / target);
+    if (split_blocks < 2) split_blocks = maxblk < 2 ? maxblk : 2;
+  }
+  if (split_blocks < 1) split_blocks = 1;
+  if (split_blocks > kMaxSplitBlocks) split_blocks = kMaxSplitBlocks;
+  int S = (maxblk + split_blocks - 1) / split_blocks;
+  if (S > kMaxSplits) return PKV_ERR_SHAPE;
+  // re-balance so that the splits are as even as possible
+  split_blocks = (maxblk + S - 1) / S;
+  plan->split_blocks = split_blocks;
+  plan->num_splits = S;
+  if (S == 1) {
+    plan->workspace_bytes = 0;
+  } else {
+    if (static_cast<int64_t>(B) * Hkv * plan->head_groups > kMaxCounters) return PKV_ERR_SHAPE;
+    const size_t rows = static_cast<size_t>(B) * Hq * S;
+    size_t bytes = kCounterRegion;
+    bytes += align_up(rows * kHeadDim * sizeof(float), 256);
+    bytes += align_up(rows * sizeof(float), 256);
+    plan->workspace_bytes = bytes;
+  }
+  return PKV_OK;
+}
+
+int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
+                  cudaStream_t stream) {
+  if (a.B == 0) return PKV_OK;
+  CUtensorMap km, vm;
+  const int64_t slots = a.num_blocks * kBlockSize;
+  if (!encode_pool_map(&km, a.k_cache, slots, a.Hkv, kTile) ||
+      !encode_pool_map(&vm, a.v_cache, slots, a.Hkv, kTile))
+    return PKV_ERR_ARG;
+  DecodeParams prm;
+  prm.out = static_cast<__nv_bfloat16*>(a.out);
+  prm.lse = a.lse;
+  prm.q = static_cast<const __nv_bfloat16*>(a.q);
+  prm.block_tables = a.block_tables;
+  prm.context_lens = a.context_lens;
+  prm.err = err;
+  prm.B = a.B;
+  prm.Hq = a.Hq;
+  prm.Hkv = a.Hkv;
+  prm.maxblk = a.max_blocks_per_seq;
+  prm.num_splits = plan.num_splits;
+  prm.split_blocks = plan.split_blocks;
+  prm.head_groups = plan.head_groups;
+  prm.num_blocks = a.num_blocks;
+  prm.scale_log2 = a.scale * 1.4426950408889634f;
+  if (plan.num_splits > 1) {
+    const size_t rows = static_cast<size_t>(a.B) * a.Hq * plan.num_splits;
+    uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+    prm.ws_count = reinterpret_cast<unsigned*>(ws);
+    ws += kCounterRegion;
+    prm.ws_o = reinterpret_cast<float*>(ws);
+    ws += align_up(rows * kHeadDim * sizeof(float), 256);
+    prm.ws_lse = reinterpret_cast<float*>(ws);
+  } else {
+    prm.ws_o = nullptr;
+    prm.ws_lse = nullptr;
+    prm.ws_count = nullptr;
+  }
+  switch (plan.heads_per_cta) {
+    case 4: return launch_g<4>(a, plan, prm, km, vm, stream);
+    case 2: return launch_g<2>(a, plan, prm, km, vm, stream);
+    default: return launch_g<1>(a, plan, prm, km, vm, stream);
+  }
+}
+
+}  // namespace pkv

@@ -1,0 +1,93 @@
+// pkv_internal.h — host-side declarations shared by the library's translation
+// units (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+// Bits of the device error word (see pkv_get_device_error()).
+constexpr unsigned kErrIndex = 1u;    // slot / block id / length out of range
+constexpr unsigned kErrTimeout = 2u;  // a bounded wait ran out
+
+// Head dimension and block size that the kernels are built for.
+constexpr int kHeadDim = 128;
+constexpr int kBlockSize = 256;
+
+// SM count of the current device (cached per device); 0 on failure.
+int device_sm_count();
+
+// Address of the device error word on the current device; nullptr on failure.
+unsigned* device_error_word();
+
+// Tensor map over one pool tensor viewed as [slots, Hkv, D] (D innermost),
+// box = {64 elements of D, 1 head, box_rows slots}, 128-byte swizzle.
+bool encode_pool_map(CUtensorMap* map, const void* base, int64_t num_slots, int Hkv,
+                     int box_rows);
+
+struct StoreArgs {
+  const void* k;
+  const void* v;
+  int64_t k_tok_stride;
+  int64_t v_tok_stride;
+  void* k_cache;
+  void* v_cache;
+  const int32_t* slot_mapping;
+  int64_t T;
+  int row_elems;  // Hkv * D
+  int64_t num_slots;
+};
+int launch_store(const StoreArgs& a, unsigned* err, cudaStream_t stream);
+
+struct DecodeArgs {
+  void* out;
+  float* lse;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  int max_blocks_per_seq;
+  const int32_t* context_lens;
+  int B, Hq, Hkv;
+  int64_t num_blocks;
+  float scale;
+  void* workspace;
+  size_t workspace_bytes;
+  int num_splits;  // as requested (0 = automatic)
+};
+
+// Split plan of one decode call.
+struct DecodePlan {
+  int heads_per_cta;  // G: query heads that one thread block serves
+  int head_groups;    // (Hq/Hkv) / G
+  int split_blocks;   // whole KV blocks per split
+  int num_splits;     // S
+  size_t workspace_bytes;
+};
+// Returns PKV_OK and fills `plan`, or a negative status.
+int plan_decode(int B, int Hq, int Hkv, int max_blocks_per_seq, int num_splits,
+                int sm_count, DecodePlan* plan);
+int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
+                  cudaStream_t stream);
+
+struct PrefillArgs {
+  void* out;
+  float* lse;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  int max_blocks_per_seq;
+  const int32_t* cu_seqlens_q;
+  const int32_t* cu_seqlens_k;
+  int B, max_seqlen_q, max_seqlen_k, Hq, Hkv;
+  int64_t num_blocks;
+  float scale;
+};
+int launch_prefill(const PrefillArgs& a, unsigned* err, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,88 @@
+// store.cu — kv_cache_store for sm_103a.
+//
+// Operation: new K/V rows are written into the paged cache through slot_mapping
+// ("Nano-vLLM System Architecture Analysis", §2 Core Components, "Attention with
+// Paged Cache"; 256-token blocks per "Paged KV Cache").  A slot addresses one
+// contiguous [Hkv, D] row of the pool, so a token's K (and V) row is a single
+// contiguous 2*Hkv*D-byte copy.
+//
+// Design: a plain bandwidth kernel.  Consecutive threads move consecutive
+// 16-byte pieces of the same row (coalesced reads and writes); the grid is a
+// multiple of the SM count and strides over (token, K|V, piece).  Padding slots
+// (< 0) are skipped; out-of-range slots are skipped and reported.
+
+#include <cuda_bf16.h>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kStoreThreads = 256;
+
+// VEC: 16-byte pieces (8 bf16); otherwise single elements.
+template <bool VEC>
+__global__ void __launch_bounds__(kStoreThreads)
+kv_store_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+                int64_t k_stride, int64_t v_stride, uint16_t* __restrict__ k_cache,
+                uint16_t* __restrict__ v_cache, const int32_t* __restrict__ slots, int64_t T,
+                int row_elems, int64_t num_slots, unsigned* err) {
+  constexpr int kPer = VEC ? 8 : 1;
+  const int pieces = row_elems / kPer;
+  const int64_t per_token = 2 * static_cast<int64_t>(pieces);
+  const int64_t total = T * per_token;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const int64_t t = i / per_token;
+    const int rem = static_cast<int>(i - t * per_token);
+    const int which = rem >= pieces;  // 0 = K, 1 = V
+    const int piece = rem - which * pieces;
+    const int64_t s = __ldg(slots + t);
+    if (s < 0) continue;
+    if (s >= num_slots) {
+      if (piece == 0 && which == 0) record_error(err, kErrIndex);
+      continue;
+    }
+    const uint16_t* src = (which ? v + t * v_stride : k + t * k_stride) + piece * kPer;
+    uint16_t* dst = (which ? v_cache : k_cache) + s * row_elems + piece * kPer;
+    if constexpr (VEC) {
+      *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
+    } else {
+      *dst = __ldg(src);
+    }
+  }
+}
+
+}  // namespace
+
+int launch_store(const StoreArgs& a, unsigned* err, cudaStream_t stream) {
+  if (a.T == 0) return PKV_OK;
+  const bool vec = (reinterpret_cast<uintptr_t>(a.k) % 16 == 0) &&
+                   (reinterpret_cast<uintptr_t>(a.v) % 16 == 0) &&
+                   ((a.k_tok_stride * 2) % 16 == 0) && ((a.v_tok_stride * 2) % 16 == 0) &&
+                   (a.row_elems % 8 == 0);
+  const int pieces = vec ? a.row_elems / 8 : a.row_elems;
+  const int64_t total = a.T * 2 * static_cast<int64_t>(pieces);
+  int sms = device_sm_count();
+  if (sms <= 0) sms = 148;
+  int64_t blocks = (total + kStoreThreads - 1) / kStoreThreads;
+  const int64_t cap = static_cast<int64_t>(sms) * 16;
+  if (blocks > cap) blocks = cap;
+  const auto* k = static_cast<const uint16_t*>(a.k);
+  const auto* v = static_cast<const uint16_t*>(a.v);
+  auto* kc = static_cast<uint16_t*>(a.k_cache);
+  auto* vc = static_cast<uint16_t*>(a.v_cache);
+  if (vec)
+    kv_store_kernel<true><<<static_cast<unsigned>(blocks), kStoreThreads, 0, stream>>>(
+        k, v, a.k_tok_stride, a.v_tok_stride, kc, vc, a.slot_mapping, a.T, a.row_elems,
+        a.num_slots, err);
+  else
+    kv_store_kernel<false><<<static_cast<unsigned>(blocks), kStoreThreads, 0, stream>>>(
+        k, v, a.k_tok_stride, a.v_tok_stride, kc, vc, a.slot_mapping, a.T, a.row_elems,
+        a.num_slots, err);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+}
+
+}  // namespace pkv

@@ -1,0 +1,243 @@
+"""Python binding of libpkv.so (include/pkv.h): argument marshalling only.
+
+Each function takes torch tensors that already live on the GPU, checks their
+dtype / layout / device, and passes raw device pointers, sizes and the current
+CUDA stream to the C entry point of the same name.  Every step of the
+computation runs in the library's CUDA kernels; there is no fallback of any kind:
+if the shared library is missing or a call fails, an exception is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+PKV_OK = 0
+PKV_ERR_ARG = -1
+PKV_ERR_SHAPE = -2
+PKV_ERR_WORKSPACE = -3
+PKV_ERR_LAUNCH = -4
+PKV_ERR_DEVICE_INDEX = -5
+PKV_ERR_TIMEOUT = -6
+
+_lock = threading.Lock()
+_lib = None
+_workspaces = {}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status) if _lib else status}")
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libpkv.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(path)
+        P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                ctypes.c_float, ctypes.c_size_t)
+        lib.kv_cache_store.argtypes = [P, P, i64, i64, P, P, P, i64, i32, i32, i32, i64, P]
+        lib.kv_cache_store.restype = i32
+        lib.paged_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+        lib.paged_decode_workspace_bytes.restype = sz
+        lib.paged_decode_num_splits.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+        lib.paged_decode_num_splits.restype = i32
+        lib.paged_decode_attention.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32,
+                                               i32, i64, f32, P, sz, i32, P]
+        lib.paged_decode_attention.restype = i32
+        lib.paged_prefill_attention.argtypes = [P, P, P, P, P, P, i32, P, P, i32, i32, i32,
+                                                i32, i32, i32, i32, i64, f32, P]
+        lib.paged_prefill_attention.restype = i32
+        lib.pkv_get_device_error.argtypes = [P]
+        lib.pkv_get_device_error.restype = i32
+        lib.pkv_status_string.argtypes = [i32]
+        lib.pkv_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().pkv_status_string(int(status)).decode()
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: Optional[int] = None,
+          contiguous: bool = True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _pool_dims(k_cache: torch.Tensor, v_cache: torch.Tensor):
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    NB, bs, Hkv, D = k_cache.shape
+    return NB, bs, Hkv, D
+
+
+def _check(status: int, what: str):
+    if status != PKV_OK:
+        raise PkvError(status, what)
+
+
+def kv_cache_store(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
+                   v_cache: torch.Tensor, slot_mapping: torch.Tensor, stream=None) -> None:
+    """k, v: bf16 [T, Hkv, D] (each token's [Hkv, D] contiguous; token stride
+    free); caches [NB, bs, Hkv, D]; slot_mapping int32 [T]."""
+    lib = load_library()
+    NB, bs, Hkv, D = _pool_dims(k_cache, v_cache)
+    for name, t in (("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, 3, contiguous=False)
+        if tuple(t.shape[1:]) != (Hkv, D) or t.stride(2) != 1 or t.stride(1) != D:
+            raise ValueError(f"{name} must be [T, {Hkv}, {D}] with contiguous rows")
+    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    T = k.shape[0]
+    if v.shape[0] != T or slot_mapping.shape[0] != T:
+        raise ValueError("k, v and slot_mapping disagree on T")
+    _check(lib.kv_cache_store(_ptr(k), _ptr(v), k.stride(0), v.stride(0), _ptr(k_cache),
+                              _ptr(v_cache), _ptr(slot_mapping), T, Hkv, D, bs, NB,
+                              _stream(stream)), "kv_cache_store")
+
+
+def paged_decode_workspace_bytes(B: int, Hq: int, Hkv: int, D: int, max_blocks_per_seq: int,
+                                 block_size: int = 256, num_splits: int = 0) -> int:
+    return int(load_library().paged_decode_workspace_bytes(B, Hq, Hkv, D, max_blocks_per_seq,
+                                                           block_size, num_splits))
+
+
+def paged_decode_num_splits(B: int, Hq: int, Hkv: int, D: int, max_blocks_per_seq: int,
+                            block_size: int = 256, num_splits: int = 0) -> int:
+    n = load_library().paged_decode_num_splits(B, Hq, Hkv, D, max_blocks_per_seq, block_size,
+                                               num_splits)
+    _check(min(n, 0), "paged_decode_num_splits")
+    return int(n)
+
+
+def decode_workspace(nbytes: int, device) -> torch.Tensor:
+    """A zero-initialised, 256-byte aligned workspace of at least nbytes on
+    `device`, reused across calls on that device (the library leaves its
+    counters zeroed).  Callers running decode concurrently on several streams
+    must pass their own workspaces instead."""
+    dev = torch.device(device)
+    key = (dev.type, dev.index if dev.index is not None else torch.cuda.current_device())
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        _workspaces[key] = ws
+    return ws
+
+
+def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor,
+                           scale: float, out: Optional[torch.Tensor] = None,
+                           lse: Optional[torch.Tensor] = None,
+                           workspace: Optional[torch.Tensor] = None, num_splits: int = 0,
+                           want_lse: bool = True, stream=None
+                           ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """q bf16 [B, Hq, D]; block_tables int32 [B, max_blocks]; context_lens int32
+    [B].  Returns (out bf16 [B, Hq, D], lse fp32 [B, Hq] or None)."""
+    lib = load_library()
+    NB, bs, Hkv, D = _pool_dims(k_cache, v_cache)
+    _need(q, "q", torch.bfloat16, 3)
+    B, Hq, Dq = q.shape
+    if Dq != D:
+        raise ValueError("q head_dim differs from the cache's")
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables / context_lens batch differs from q")
+    maxblk = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    need = paged_decode_workspace_bytes(B, Hq, Hkv, D, maxblk, bs, num_splits)
+    if workspace is None and need:
+        workspace = decode_workspace(need, q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.paged_decode_attention(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache),
+                                      _ptr(v_cache), _ptr(block_tables), maxblk,
+                                      _ptr(context_lens), B, Hq, Hkv, D, bs, NB, float(scale),
+                                      _ptr(workspace), ws_bytes, int(num_splits),
+                                      _stream(stream)), "paged_decode_attention")
+    return out, lse
+
+
+def paged_prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                            cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int,
+                            scale: float, out: Optional[torch.Tensor] = None,
+                            lse: Optional[torch.Tensor] = None, want_lse: bool = True,
+                            stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """q bf16 [sum Lq, Hq, D]; cu_seqlens int32 [B+1].  The new tokens' K/V must
+    already be stored in the pool.  Returns (out bf16 [sum Lq, Hq, D], lse fp32
+    [sum Lq, Hq] or None)."""
+    lib = load_library()
+    NB, bs, Hkv, D = _pool_dims(k_cache, v_cache)
+    _need(q, "q", torch.bfloat16, 3)
+    Nq, Hq, Dq = q.shape
+    if Dq != D:
+        raise ValueError("q head_dim differs from the cache's")
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    B = cu_seqlens_q.shape[0] - 1
+    if cu_seqlens_k.shape[0] != B + 1 or block_tables.shape[0] != B:
+        raise ValueError("cu_seqlens / block_tables batch sizes differ")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse is None and want_lse:
+        lse = torch.empty((Nq, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    _check(lib.paged_prefill_attention(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache),
+                                       _ptr(v_cache), _ptr(block_tables),
+                                       block_tables.shape[1], _ptr(cu_seqlens_q),
+                                       _ptr(cu_seqlens_k), B, int(max_seqlen_q),
+                                       int(max_seqlen_k), Hq, Hkv, D, bs, NB, float(scale),
+                                       _stream(stream)), "paged_prefill_attention")
+    return out, lse
+
+
+def get_device_error(stream=None) -> int:
+    """Synchronise the stream and read-and-clear the device error word."""
+    return int(load_library().pkv_get_device_error(_stream(stream)))

@@ -1,0 +1,79 @@
+"""The C-ABI library loads and exports every symbol include/pkv.h declares; host
+argument checks answer without touching a GPU (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_214_gb300 import build as B
+from paged_kv_cache_214_gb300 import pkv
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "pkv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:int|size_t|const char\s*\*)\s*(\w+)\s*\(", text, flags=re.M)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return pkv.load_library()
+
+
+def test_header_declares_the_hot_path():
+    names = declared_functions()
+    for n in ("kv_cache_store", "paged_decode_attention", "paged_prefill_attention",
+              "paged_decode_workspace_bytes", "pkv_get_device_error", "pkv_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_host_argument_checks(lib):
+    s = None
+    # negative T, unsupported head_dim / block size, head counts
+    assert lib.kv_cache_store(None, None, 0, 0, None, None, None, -1, 8, 128, 256, 16, s) == pkv.PKV_ERR_ARG
+    assert lib.kv_cache_store(None, None, 0, 0, None, None, None, 0, 8, 64, 256, 16, s) == pkv.PKV_ERR_SHAPE
+    assert lib.kv_cache_store(None, None, 0, 0, None, None, None, 0, 8, 128, 16, 16, s) == pkv.PKV_ERR_SHAPE
+    assert lib.kv_cache_store(None, None, 0, 0, None, None, None, 0, 8, 128, 256, 16, s) == pkv.PKV_OK
+    assert lib.kv_cache_store(None, None, 1024, 1024, None, None, None, 4, 8, 128, 256, 16, s) == pkv.PKV_ERR_ARG
+    assert lib.paged_decode_attention(None, None, None, None, None, None, 1, None, 2, 12, 8, 128,
+                                      256, 16, 1.0, None, 0, 0, s) == pkv.PKV_ERR_SHAPE
+    assert lib.paged_decode_attention(None, None, None, None, None, None, 1, None, 0, 16, 8, 128,
+                                      256, 16, 1.0, None, 0, 0, s) == pkv.PKV_OK
+    assert lib.paged_decode_attention(None, None, None, None, None, None, 1, None, 2, 16, 8, 128,
+                                      256, 16, 1.0, None, 0, 0, s) == pkv.PKV_ERR_ARG
+    assert lib.paged_prefill_attention(None, None, None, None, None, None, 1, None, None, 2, 8,
+                                       8, 16, 8, 64, 256, 16, 1.0, s) == pkv.PKV_ERR_SHAPE
+    assert lib.paged_prefill_attention(None, None, None, None, None, None, 1, None, None, 2, 8,
+                                       8, 16, 8, 128, 256, 16, 1.0, s) == pkv.PKV_ERR_ARG
+    # pools whose slot count does not fit 32-bit TMA coordinates
+    assert lib.kv_cache_store(None, None, 0, 0, None, None, None, 0, 8, 128, 256, 1 << 24, s) == pkv.PKV_ERR_SHAPE
+
+
+def test_workspace_query_and_split_plan(lib):
+    # one split needs no workspace; several need partials + counters
+    assert pkv.paged_decode_workspace_bytes(4, 16, 8, 128, 1, 256, 1) == 0
+    ws = pkv.paged_decode_workspace_bytes(8, 32, 8, 128, 512, 256, 16)
+    assert ws >= (1 << 20) + 8 * 32 * 16 * (128 * 4 + 4)
+    assert pkv.paged_decode_num_splits(8, 32, 8, 128, 512, 256, 16) == 16
+    assert pkv.paged_decode_num_splits(8, 32, 8, 128, 64, 256, 7) == 7
+    # a requested count is raised so that no split exceeds 32 blocks
+    assert pkv.paged_decode_num_splits(8, 32, 8, 128, 512, 256, 7) == 16
+    assert pkv.paged_decode_workspace_bytes(8, 32, 8, 64, 512, 256, 16) == 0   # rejected shape
+    with pytest.raises(pkv.PkvError):
+        pkv.paged_decode_num_splits(8, 32, 8, 64, 512, 256, 0)
+
+
+def test_status_strings(lib):
+    for code in range(-6, 1):
+        assert pkv.status_string(code).startswith("PKV_")
+    assert "unknown" in pkv.status_string(42)

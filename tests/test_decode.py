@@ -1,0 +1,154 @@
+"""paged_decode_attention on the GPU against the oracle (max|dout| <= 1e-2,
+max|dlse| <= 1e-3), including the store of the step's new token."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import assert_close, bits, compact_pool
+from paged_kv_cache_214_gb300 import pkv
+from paged_kv_cache_214_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def run_and_check(w, num_splits=0, sample=None, what=""):
+    """Store the new tokens then decode on the GPU; the oracle repeats the store
+    and decode on host copies of the original inputs.  `sample`: indices of the
+    sequences the oracle checks (all by default)."""
+    dev = "cuda"
+    kc, vc = w.k_cache.to(dev), w.v_cache.to(dev)
+    seqs = list(range(w.B)) if sample is None else list(sample)
+    tables = w.block_tables[seqs]
+    kh, vh, th = compact_pool(kc, vc, tables)      # before any library kernel runs
+    slot_host = w.slot_mapping[seqs].clone()
+    # slots of the sampled sequences, renumbered to the compact copy
+    used = tables[tables >= 0].unique()
+    remap = {int(b): i for i, b in enumerate(used)}
+    bs = w.block_size
+    slot_host = torch.tensor([remap[int(s) // bs] * bs + int(s) % bs if s >= 0 else -1
+                              for s in slot_host], dtype=torch.int32)
+    pkv.kv_cache_store(w.k_new.to(dev), w.v_new.to(dev), kc, vc, w.slot_mapping.to(dev))
+    out, lse = pkv.paged_decode_attention(w.q.to(dev), kc, vc, w.block_tables.to(dev),
+                                          w.context_lens.to(dev), w.scale,
+                                          num_splits=num_splits)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == pkv.PKV_OK
+    oracle.store(bits(w.k_new[seqs]), bits(w.v_new[seqs]), kh, vh, slot_host.numpy())
+    ref_o, ref_l = oracle.decode(bits(w.q[seqs]), kh, vh, th, w.context_lens[seqs].numpy(),
+                                 w.scale)
+    return assert_close(out[seqs], lse[seqs], ref_o, ref_l, what)
+
+
+def test_tiny_decode_workload():
+    run_and_check(W.config_workload(1), what="tiny-decode")
+
+
+@pytest.mark.parametrize("num_splits", [1, 2, 3, 7, 0, 64])
+def test_forced_splits(num_splits):
+    lens = [1, 17, 255, 256, 257, 600, 1000, 4095, 4096, 4097]
+    w = W.make_decode(lens, 16, 8, 96, 1000 + num_splits)
+    run_and_check(w, num_splits=num_splits, what=f"S={num_splits}")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 8), (32, 8), (24, 8), (64, 8), (4, 1), (14, 2)])
+def test_head_groupings(Hq, Hkv):
+    lens = [5, 64, 130, 700, 2000]
+    w = W.make_decode(lens, Hq, Hkv, 24, 2000 + Hq * 10 + Hkv)
+    run_and_check(w, what=f"Hq={Hq},Hkv={Hkv}")
+
+
+def test_ragged_tile_tails():
+    # every residue of the 64-token tile and of the 256-token block
+    lens = [1, 2, 63, 64, 65, 127, 128, 129, 191, 192, 193, 255, 256, 257, 511, 512, 513]
+    w = W.make_decode(lens, 32, 8, 64, 3000)
+    run_and_check(w, num_splits=0, what="tails")
+    run_and_check(w, num_splits=2, what="tails S=2")
+
+
+def test_empty_context_gives_zero_and_neg_inf():
+    w = W.make_decode([0, 300, 0], 16, 8, 8, 3100, store_new_token=False)
+    dev = "cuda"
+    out, lse = pkv.paged_decode_attention(w.q.to(dev), w.k_cache.to(dev), w.v_cache.to(dev),
+                                          w.block_tables.to(dev), w.context_lens.to(dev),
+                                          w.scale, num_splits=2)
+    torch.cuda.synchronize()
+    assert (out[0] == 0).all() and (out[2] == 0).all()
+    assert torch.isneginf(lse[0]).all() and torch.isneginf(lse[2]).all()
+    assert torch.isfinite(lse[1]).all()
+
+
+def test_repeated_calls_share_workspace():
+    """The arrival counters are reset by every call: the same inputs give the
+    same bits call after call."""
+    w = W.make_decode([3000, 5000, 100], 32, 8, 64, 3200, store_new_token=False)
+    dev = "cuda"
+    args = (w.q.to(dev), w.k_cache.to(dev), w.v_cache.to(dev), w.block_tables.to(dev),
+            w.context_lens.to(dev), w.scale)
+    o1, l1 = pkv.paged_decode_attention(*args, num_splits=5)
+    o1, l1 = o1.clone(), l1.clone()
+    for _ in range(3):
+        o2, l2 = pkv.paged_decode_attention(*args, num_splits=5)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_one_workspace_serves_every_shape():
+    """Calls of different shapes share one workspace: each call's partials never
+    overwrite the counters of another shape."""
+    dev = "cuda"
+    ws = torch.zeros(64 << 20, dtype=torch.uint8, device=dev)
+    cases = [W.make_decode([3000, 900, 5000], 32, 8, 64, 3500, store_new_token=False),
+             W.make_decode([700, 4000], 24, 8, 64, 3501, store_new_token=False),
+             W.make_decode([2500, 2600, 100, 4100], 16, 8, 64, 3502, store_new_token=False)]
+    for rep in range(2):
+        for w in cases:
+            out, lse = pkv.paged_decode_attention(
+                w.q.to(dev), w.k_cache.to(dev), w.v_cache.to(dev), w.block_tables.to(dev),
+                w.context_lens.to(dev), w.scale, workspace=ws, num_splits=3 + rep)
+            torch.cuda.synchronize()
+            ref_o, ref_l = oracle.decode(bits(w.q), bits(w.k_cache), bits(w.v_cache),
+                                         w.block_tables.numpy(), w.context_lens.numpy(), w.scale)
+            assert_close(out, lse, ref_o, ref_l, f"shared workspace rep {rep}")
+
+
+def test_decode_b64_full():
+    run_and_check(W.config_workload(2, pool_device="cuda"), what="decode-b64")
+
+
+def test_prefix_shared_b256_sampled():
+    w = W.config_workload(3, pool_device="cuda")
+    g = torch.Generator().manual_seed(77)
+    sample = sorted(torch.randperm(w.B, generator=g)[:12].tolist())
+    run_and_check(w, sample=sample, what="prefix-shared-b256")
+
+
+def test_long_decode_b8_sampled():
+    w = W.config_workload(5, pool_device="cuda")
+    run_and_check(w, sample=[0, 5], what="long-decode-b8")
+
+
+def test_bad_block_id_and_long_context_are_reported():
+    w = W.make_decode([300, 40], 16, 8, 8, 3300, store_new_token=False)
+    dev = "cuda"
+    bt = w.block_tables.clone()
+    bt[0, 1] = 1 << 20                   # outside the pool
+    lens = w.context_lens.clone()
+    args = (w.q.to(dev), w.k_cache.to(dev), w.v_cache.to(dev))
+    assert pkv.get_device_error() == pkv.PKV_OK
+    pkv.paged_decode_attention(*args, bt.to(dev), lens.to(dev), w.scale)
+    assert pkv.get_device_error() == pkv.PKV_ERR_DEVICE_INDEX
+    lens[1] = 10_000                     # longer than its table can address
+    pkv.paged_decode_attention(*args, w.block_tables.to(dev), lens.to(dev), w.scale)
+    assert pkv.get_device_error() == pkv.PKV_ERR_DEVICE_INDEX
+    assert pkv.get_device_error() == pkv.PKV_OK
+
+
+def test_workspace_too_small_is_rejected():
+    w = W.make_decode([3000, 5000], 32, 8, 64, 3400, store_new_token=False)
+    dev = "cuda"
+    small = torch.zeros(256, dtype=torch.uint8, device=dev)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_decode_attention(w.q.to(dev), w.k_cache.to(dev), w.v_cache.to(dev),
+                                   w.block_tables.to(dev), w.context_lens.to(dev), w.scale,
+                                   workspace=small, num_splits=4)
+    assert e.value.status == pkv.PKV_ERR_WORKSPACE
