@@ -269,7 +269,12 @@ def run_gpu(args, world, rank):
     from paged_kv_cache_214_gb300 import pkv
     dev = torch.device("cuda", torch.cuda.current_device())
     hbm_peak, _, peak_kind = _peaks()
-    w = W.config_workload(2, pool_device=dev, rotations=ROTATIONS)
+    if args.profile:
+        # same decode-b64 batch, one rotation, pool trimmed to the blocks it
+        # uses (~560 MB of K/V on the device): a small case for ncu captures
+        w = _trimmed_decode_b64(dev)
+    else:
+        w = W.config_workload(2, pool_device=dev, rotations=ROTATIONS)
     tables_h = [w.block_tables] + w.extra_tables
     slots_h = [w.slot_mapping] + w.extra_slots
     R = len(tables_h)
@@ -347,7 +352,7 @@ def run_gpu(args, world, rank):
                      "avg_launch_us": round(dec_avg_ms * 1e3, 2)},
         "clocks": clk,
     }
-    if rank == 0:
+    if rank == 0 and not args.profile:
         result["e2e"] = run_e2e(pkv, w, dev_inputs, ws, stream, K, step_bytes)
         if not args.no_extras:
             del dev_inputs, kc, vc, tables, slots, ws, out, lse
@@ -357,6 +362,13 @@ def run_gpu(args, world, rank):
         if not args.no_cpu_baseline:
             result["cpu_baseline"] = time_oracle(W.config_workload(2, pool_device=dev))
     return result
+
+
+def _trimmed_decode_b64(dev):
+    lens = W._uniform_ints(512, 4096, 64, W.seed_for(2))
+    nblk = sum(-(-x // W.BLOCK_SIZE) for x in lens)
+    return W.make_decode(lens, 16, 8, nblk, W.seed_for(2), name="decode-b64",
+                         pool_device=dev)
 
 
 def run_e2e(pkv, w, dev_inputs, ws, stream, K, step_bytes):
@@ -600,9 +612,15 @@ def main():
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="small-footprint run for ncu: one batch, trimmed pool, "
+                         "no extras / e2e / CPU baseline")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.profile:
+        args.no_extras = True
+        args.no_cpu_baseline = True
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         res = run_reference(args, world, rank)
