@@ -133,6 +133,42 @@ int paged_decode_attention(void* out, float* lse, const void* q,
                            void* workspace, size_t workspace_bytes,
                            int num_splits, pkv_stream_t stream);
 
+/* Size of the fixed device scratch array behind
+ * paged_decode_attention_noalloc (16 MiB per device that loads the library). */
+#define PKV_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/* paged_decode_attention_noalloc — the same decode attention as
+ * paged_decode_attention, for callers that cannot allocate device memory and so
+ * cannot provide its workspace: for example a plugin whose host framework owns
+ * every device allocation and passes the library only its input and output
+ * tensors, or a runtime with a fixed memory plan in which no call may
+ * allocate.  The source pages have no counterpart to this call; it exists only
+ * for such callers.
+ *
+ * Arguments, layouts, results and errors are those of paged_decode_attention
+ * without the workspace arguments.  The split partials and arrival counters
+ * live in a scratch array inside the library, PKV_NOALLOC_SCRATCH_BYTES long,
+ * which every GPU that loads the library holds until the process exits.  The
+ * call allocates nothing: it uses no cudaMalloc, cudaFree or allocating
+ * library routine.
+ *   - A call whose partials would not fit in that array (see
+ *     paged_decode_workspace_bytes: it must be <= PKV_NOALLOC_SCRATCH_BYTES)
+ *     returns PKV_ERR_WORKSPACE and launches nothing.
+ *   - The first call on a device looks up the array's device address once
+ *     (cudaGetSymbolAddress) and caches it; make that first call before any
+ *     stream capture starts on that device.
+ *   - Every call on a device uses the same array, which keeps the previous
+ *     call's contents; each call clears its own arrival counters (an async
+ *     memset on `stream`) before its kernel.  Calls whose work overlaps on the
+ *     GPU (different streams not ordered by events, or several host threads)
+ *     race on the array and give wrong results: order them. */
+int paged_decode_attention_noalloc(void* out, float* lse, const void* q,
+                                   const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* context_lens, int B, int Hq, int Hkv,
+                                   int D, int block_size, int64_t num_blocks, float scale,
+                                   int num_splits, pkv_stream_t stream);
+
 /* paged_prefill_attention — causal prefill / chunked prefill with a prefix
  * cache: "During prefill with prefix cache, gathers cached K/V from the paged
  * cache and concatenates with newly computed ones" (Nano-vLLM System

@@ -60,6 +60,9 @@ def load_library(path: str = LIB_PATH):
         lib.paged_decode_attention.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32,
                                                i32, i64, f32, P, sz, i32, P]
         lib.paged_decode_attention.restype = i32
+        lib.paged_decode_attention_noalloc.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32,
+                                                       i32, i32, i64, f32, i32, P]
+        lib.paged_decode_attention_noalloc.restype = i32
         lib.paged_prefill_attention.argtypes = [P, P, P, P, P, P, i32, P, P, i32, i32, i32,
                                                 i32, i32, i32, i32, i64, f32, P]
         lib.paged_prefill_attention.restype = i32
@@ -199,6 +202,33 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                                       _ptr(workspace), ws_bytes, int(num_splits),
                                       _stream(stream)), "paged_decode_attention")
     return out, lse
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def paged_decode_attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor,
+                                   v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                   context_lens: torch.Tensor, scale: float,
+                                   out: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                                   num_splits: int = 0, stream=None) -> None:
+    """Decode attention for callers that cannot allocate device memory: the
+    split scratch is a fixed 16 MiB array inside the library instead of a
+    caller-provided workspace, and the caller passes `out` (and optionally
+    `lse`) already allocated.  Calls that overlap on the GPU race on that array."""
+    lib = load_library()
+    NB, bs, Hkv, D = _pool_dims(k_cache, v_cache)
+    _need(q, "q", torch.bfloat16, 3)
+    B, Hq, _ = q.shape
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    _check(lib.paged_decode_attention_noalloc(
+        _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), B, Hq, Hkv, D, bs, NB, float(scale),
+        int(num_splits), _stream(stream)), "paged_decode_attention_noalloc")
 
 
 def paged_prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
