@@ -604,6 +604,34 @@ def run_reference(args, world, rank):
     }
 
 
+def run_prefill_profile(args):
+    """Small-footprint prefill run for ncu: chunked-prefill-b16 (store of the
+    8192 new tokens, then prefill), warmup + steps calls, one JSON line."""
+    from paged_kv_cache_214_gb300 import pkv
+    dev = torch.device("cuda", torch.cuda.current_device())
+    # chunked-prefill-b16 shapes with the pool trimmed to the 96 blocks it uses
+    w = W.make_prefill([1024] * 16, [512] * 16, 32, 8, 96, W.seed_for(4),
+                       name="chunked-prefill-b16", pool_device=dev)
+    q, kc, vc = w.q.to(dev), w.k_cache, w.v_cache
+    kn, vn, slots = w.k_new.to(dev), w.v_new.to(dev), w.slot_mapping.to(dev)
+    tables, cq, ck = w.block_tables.to(dev), w.cu_seqlens_q.to(dev), w.cu_seqlens_k.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((q.shape[0], w.Hq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    pkv.kv_cache_store(kn, vn, kc, vc, slots, stream=stream)
+
+    def call():
+        pkv.paged_prefill_attention(q, kc, vc, tables, cq, ck, w.max_seqlen_q, w.max_seqlen_k,
+                                    w.scale, out=out, lse=lse, stream=stream)
+    for _ in range(args.warmup):
+        call()
+    med, mn = _time_calls(call, args.steps, stream)
+    assert pkv.get_device_error() == pkv.PKV_OK
+    fl = prefill_flops(w)
+    print(json.dumps({"workload": w.name, "prefill_us": round(med * 1e3, 2),
+                      "TFLOP/s": round(fl / (med / 1e3) / 1e12, 1)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -612,6 +640,8 @@ def main():
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-kernel", choices=["decode", "prefill"], default="decode",
+                    help="with --profile: which kernel the run exercises")
     ap.add_argument("--profile", action="store_true",
                     help="small-footprint run for ncu: one batch, trimmed pool, "
                          "no extras / e2e / CPU baseline")
@@ -622,6 +652,9 @@ def main():
         args.no_extras = True
         args.no_cpu_baseline = True
     world, rank, local = dist_setup(args)
+    if args.profile_kernel == "prefill":
+        run_prefill_profile(args)
+        return
     if args.impl == "reference":
         res = run_reference(args, world, rank)
     else:
