@@ -12,15 +12,18 @@
 //   (sequence, kv head, range of whole KV blocks) and serves the G query heads
 //   of that kv head's group that it is assigned, so each K/V byte is read from
 //   HBM once per G heads.
-//   Warp 4 (producer): lane 0 streams the range's K and V through a 3-stage
-//   ring of shared-memory tiles with TMA (64 tokens x 128 dims per tile; two
-//   64-dim boxes per operand, 128-byte swizzle) and mbarrier completion.
-//   Warps 0-3 (consumers): sixteen 8-lane groups, each an independent online
+//   The range's K and V stream through a 3-stage ring of shared-memory tiles
+//   with TMA (64 tokens x 128 dims per tile; two 64-dim boxes per operand,
+//   128-byte swizzle) and mbarrier completion; lane 0 of warp 0 issues the
+//   copies, refilling a stage as soon as all four warps have released it.
+//   Four warps (two blocks per SM, so up to 255 registers a thread): sixteen
+//   8-lane groups, each an independent online
 //   softmax stream.  Lane j of a group owns dims [8j, 8j+8) and [64+8j, 64+8j+8)
 //   of q and of the running output for all G heads, all in registers.  A group
-//   takes one token row per step: 16 partial products per head, a 3-level
-//   butterfly to finish the dot product, then the running max / sum update and
-//   o += p * v on the same 16 dims.
+//   takes one token row per step: 16 partial products per head (8 packed
+//   fp32x2 FMAs), a 3-level butterfly to finish the dot product, then, once
+//   per tile, the running max / sum update and o += p * v on the same 16 dims
+//   (8 packed FMAs per head).
 //   End of the range: the 16 streams are merged by log-sum-exp (shuffles
 //   across the groups of a warp, then shared memory across warps).
 //   With one split the block writes out/lse directly.  Otherwise it writes a
@@ -43,7 +46,7 @@ namespace {
 constexpr int kTile = 64;                       // tokens per pipeline stage
 constexpr int kStages = 3;
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kThreads = kConsumerWarps * 32;
 constexpr int kHalfBytes = kTile * 128;         // 64 rows x 64 dims x 2 B
 constexpr int kOperandBytes = 2 * kHalfBytes;   // one of K or V for a tile
 constexpr int kStageBytes = 2 * kOperandBytes;  // K and V
@@ -82,13 +85,6 @@ struct SmemLayout {
   static constexpr int kEnd = kFlags + 16;
   static constexpr int kBytes = kEnd + 1024;                                 // + alignment slack
 };
-
-__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
-  f[0] = bf16lo(u.x); f[1] = bf16hi(u.x);
-  f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
-  f[4] = bf16lo(u.z); f[5] = bf16hi(u.z);
-  f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
-}
 
 // Weight of a stream with log2-max m against the common max mn (0 for an
 // empty stream).
@@ -156,12 +152,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     flags[1] = 0;  // last-arrival flag
     flags[2] = 0;  // tiles issued
     fence_barrier_init();
+    tma_prefetch_map(&kmap);
+    tma_prefetch_map(&vmap);
   }
-  if (warp == kConsumerWarps) {
-    if (lane == 0) {
-      tma_prefetch_map(&kmap);
-      tma_prefetch_map(&vmap);
-    }
+  if (warp == 0) {
     // Block ids of this range (validated; a bad id is reported and replaced by
     // block 0 so that no out-of-range address is ever formed).
     const int nblk = (tok_end - 1) / kBlockSize - blk_begin + 1;
@@ -176,54 +170,51 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   }
   __syncthreads();
 
-  if (warp == kConsumerWarps) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t policy = l2_policy_evict_first();
-      int it = 0;
-      for (; it < n_tiles; ++it) {
-        const int s = it % kStages;
-        if (it >= kStages && !mbar_wait(empty_bar(s), ((it / kStages) - 1) & 1)) {
-          record_error(p.err, kErrTimeout);
-          flags[0] = 1;
-          break;
-        }
-        if (flags[0]) break;
-        const int tok = tok_begin + it * kTile;
-        const int slot = sblk[tok / kBlockSize - blk_begin] * kBlockSize + tok % kBlockSize;
-        const uint32_t kdst = smem_addr(smem + s * kStageBytes);
-        const uint32_t vdst = kdst + kOperandBytes;
-        mbar_arrive_expect_tx(full_bar(s), kStageBytes);
-        tma_load_3d_hint(kdst, &kmap, full_bar(s), 0, kvh, slot, policy);
-        tma_load_3d_hint(kdst + kHalfBytes, &kmap, full_bar(s), 64, kvh, slot, policy);
-        tma_load_3d_hint(vdst, &vmap, full_bar(s), 0, kvh, slot, policy);
-        tma_load_3d_hint(vdst + kHalfBytes, &vmap, full_bar(s), 64, kvh, slot, policy);
-      }
-      flags[2] = it;
-    }
-  } else {
+  // Lane 0 of warp 0 is the producer: it fills the ring up front and refills a
+  // stage as soon as all four warps have released it.
+  const uint64_t policy = l2_policy_evict_first();
+  auto issue = [&](int it) {
+    const int s = it % kStages;
+    const int tok = tok_begin + it * kTile;
+    const int slot = sblk[tok / kBlockSize - blk_begin] * kBlockSize + tok % kBlockSize;
+    const uint32_t kdst = smem_addr(smem + s * kStageBytes);
+    const uint32_t vdst = kdst + kOperandBytes;
+    mbar_arrive_expect_tx(full_bar(s), kStageBytes);
+    tma_load_3d_hint(kdst, &kmap, full_bar(s), 0, kvh, slot, policy);
+    tma_load_3d_hint(kdst + kHalfBytes, &kmap, full_bar(s), 64, kvh, slot, policy);
+    tma_load_3d_hint(vdst, &vmap, full_bar(s), 0, kvh, slot, policy);
+    tma_load_3d_hint(vdst + kHalfBytes, &vmap, full_bar(s), 64, kvh, slot, policy);
+    flags[2] = it + 1;
+  };
+  if (tid == 0) {
+    for (int it = 0; it < kStages && it < n_tiles; ++it) issue(it);
+  }
+
+  {
     // ------------------------------------------------------------ consumers
     const int grp = lane >> 3;  // group within the warp
     const int j = lane & 7;     // lane within the group: dims [8j,8j+8) and [64+8j,64+8j+8)
-    float qf[G][16];
+    // q (pre-scaled into base-2 units) and the running output, as fp32 pairs:
+    // pair i < 4 covers dims 8j+2i, 8j+2i+1; pair i >= 4 covers 64+8j+2(i-4), +1.
+    f32x2 q2[G][8];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const __nv_bfloat16* qp = p.q + (static_cast<int64_t>(b) * p.Hq + h0 + h) * kHeadDim;
       const uint4 a = __ldg(reinterpret_cast<const uint4*>(qp + 8 * j));
       const uint4 c = __ldg(reinterpret_cast<const uint4*>(qp + 64 + 8 * j));
-      unpack8(a, &qf[h][0]);
-      unpack8(c, &qf[h][8]);
+      const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+      const f32x2 sc2 = pack2(p.scale_log2, p.scale_log2);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) qf[h][i] *= p.scale_log2;
+      for (int i = 0; i < 8; ++i) q2[h][i] = mul2(bf16x2_to_f32x2(w[i]), sc2);
     }
-    float o[G][16];
+    f32x2 o2[G][8];
     float m[G], l[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       m[h] = -INFINITY;
       l[h] = 0.f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) o[h][i] = 0.f;
+      for (int i = 0; i < 8; ++i) o2[h][i] = 0ull;
     }
 
     for (int it = 0; it < n_tiles; ++it) {
@@ -238,45 +229,54 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       const uint32_t kb = smem_addr(smem + s * kStageBytes);
       const uint32_t vb = kb + kOperandBytes;
 
+      // scores of this group's four rows of the tile, base-2 units
       float sc[4][G];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int t = 16 * r + 4 * warp + grp;
         const uint32_t off = t * 128 + ((j ^ (t & 7)) << 4);
-        float kf[16];
-        unpack8(lds128(kb + off), &kf[0]);
-        unpack8(lds128(kb + kHalfBytes + off), &kf[8]);
+        const uint4 k0 = lds128(kb + off);
+        const uint4 k1 = lds128(kb + kHalfBytes + off);
+        const uint32_t w[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+        f32x2 kf[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) kf[i] = bf16x2_to_f32x2(w[i]);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          float a0 = 0.f, a1 = 0.f;
+          f32x2 a0 = mul2(q2[h][0], kf[0]);
+          f32x2 a1 = mul2(q2[h][1], kf[1]);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            a0 = fmaf(qf[h][i], kf[i], a0);
-            a1 = fmaf(qf[h][8 + i], kf[8 + i], a1);
+          for (int i = 2; i < 8; i += 2) {
+            a0 = fma2(q2[h][i], kf[i], a0);
+            a1 = fma2(q2[h][i + 1], kf[i + 1], a1);
           }
-          float acc = a0 + a1;
+          a0 = add2(a0, a1);
+          float acc = lo2(a0) + hi2(a0);
           acc += __shfl_xor_sync(0xffffffffu, acc, 1);
           acc += __shfl_xor_sync(0xffffffffu, acc, 2);
           acc += __shfl_xor_sync(0xffffffffu, acc, 4);
           sc[r][h] = t < n_valid ? acc : -INFINITY;
         }
       }
-      // online softmax update, once per tile
+      // online softmax, once per tile.  The running max only moves when the
+      // tile's max exceeds it by more than 2^8; below that the stale max is
+      // kept (weights up to 256 are exact enough in fp32) and o is not rescaled.
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float mt = fmaxf(fmaxf(sc[0][h], sc[1][h]), fmaxf(sc[2][h], sc[3][h]));
-        const float mn = fmaxf(m[h], mt);
-        if (mn != -INFINITY) {
-          const float alpha = rescale(m[h], mn);
+        if (mt > m[h] + 8.f) {
+          const float alpha = rescale(m[h], mt);
           l[h] *= alpha;
+          const f32x2 a2 = pack2(alpha, alpha);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) o[h][i] *= alpha;
-          m[h] = mn;
+          for (int i = 0; i < 8; ++i) o2[h][i] = mul2(o2[h][i], a2);
+          m[h] = mt;
+        }
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            sc[r][h] = ex2(sc[r][h] - mn);  // -inf -> 0
-            l[h] += sc[r][h];
-          }
+        for (int r = 0; r < 4; ++r) {
+          const int t = 16 * r + 4 * warp + grp;
+          sc[r][h] = t < n_valid ? ex2(sc[r][h] - m[h]) : 0.f;
+          l[h] += sc[r][h];
         }
       }
 #pragma unroll
@@ -284,18 +284,43 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         const int t = 16 * r + 4 * warp + grp;
         if (t < n_valid) {
           const uint32_t off = t * 128 + ((j ^ (t & 7)) << 4);
-          float vf[16];
-          unpack8(lds128(vb + off), &vf[0]);
-          unpack8(lds128(vb + kHalfBytes + off), &vf[8]);
+          const uint4 v0 = lds128(vb + off);
+          const uint4 v1 = lds128(vb + kHalfBytes + off);
+          const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+          f32x2 vf[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) vf[i] = bf16x2_to_f32x2(w[i]);
 #pragma unroll
           for (int h = 0; h < G; ++h) {
+            const f32x2 p2 = pack2(sc[r][h], sc[r][h]);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) o[h][i] = fmaf(sc[r][h], vf[i], o[h][i]);
+            for (int i = 0; i < 8; ++i) o2[h][i] = fma2(p2, vf[i], o2[h][i]);
           }
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty_bar(s));
+      if (lane == 0) {
+        mbar_arrive(empty_bar(s));
+        if (warp == 0 && it + kStages < n_tiles && !flags[0]) {
+          if (mbar_wait(empty_bar(s), (it / kStages) & 1)) {
+            issue(it + kStages);
+          } else {
+            record_error(p.err, kErrTimeout);
+            flags[0] = 1;
+          }
+        }
+      }
+      __syncwarp();
+    }
+
+    float o[G][16];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        o[h][2 * i] = lo2(o2[h][i]);
+        o[h][2 * i + 1] = hi2(o2[h][i]);
+      }
     }
 
     // merge the four groups of this warp (lanes j, j+8, j+16, j+24)
@@ -342,7 +367,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       if (last >= 0) (void)mbar_wait(full_bar(s), (last / kStages) & 1);
     }
   }
-  if (warp == kConsumerWarps) return;
 
   // ---------------------------------------------------------------- epilogue
   // thread tid (0..127) owns dim d = tid of every head
