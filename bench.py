@@ -486,6 +486,38 @@ def run_extras(pkv, dev, hbm_peak, args):
             entry["unique_frac_of_peak"] = round(ub / hbm_peak, 4)
             entry["note"] = ("GB/s counts the shared prefix once per sequence (logical); "
                              "unique_GB/s counts it once")
+            # the same batch through the shared-prefix entry point
+            P = w.shared_prefix_blocks * w.block_size
+            need = pkv.paged_decode_shared_prefix_workspace_bytes(w.B, w.Hq, w.Hkv, w.D,
+                                                                  tables.shape[1], P)
+            ws2 = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+
+            def call_sp():
+                pkv.paged_decode_attention_shared_prefix(q, kc, vc, tables, lens, w.scale, P,
+                                                         out=out, lse=lse, workspace=ws2,
+                                                         stream=stream)
+            for _ in range(5):
+                call_sp()
+            times = []
+            for _ in range(30):
+                _flush_l2(flush)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                call_sp()
+                b.record(stream)
+                times.append((a, b))
+            torch.cuda.synchronize()
+            ms2 = sorted(x.elapsed_time(y) for x, y in times)
+            med2 = ms2[len(ms2) // 2]
+            ub2 = decode_bytes(w, unique=True) / (med2 / 1e3) / 1e9
+            entry["shared_prefix_path"] = {
+                "median_us": round(med2 * 1e3, 2), "min_us": round(ms2[0] * 1e3, 2),
+                "unique_GB/s": round(ub2, 1), "unique_frac_of_peak": round(ub2 / hbm_peak, 4),
+                "kv_tokens_per_s": round(w.kv_tokens / (med2 / 1e3), 1),
+                "note": "paged_decode_attention_shared_prefix: the 2048-token prefix "
+                        "attended once per kv head on tcgen05, then split decode of the "
+                        "private suffixes"}
+            del ws2
         if cfg == 1:
             g = torch.cuda.CUDAGraph()
             s2 = torch.cuda.Stream()

@@ -133,6 +133,49 @@ int paged_decode_attention(void* out, float* lse, const void* q,
                            void* workspace, size_t workspace_bytes,
                            int num_splits, pkv_stream_t stream);
 
+/* paged_decode_shared_prefix_workspace_bytes — workspace bytes that a
+ * paged_decode_attention_shared_prefix call with the same arguments needs
+ * (0 for arguments that call would reject). */
+size_t paged_decode_shared_prefix_workspace_bytes(int B, int Hq, int Hkv, int D,
+                                                  int max_blocks_per_seq, int block_size,
+                                                  int shared_prefix_tokens, int num_splits);
+
+/* paged_decode_attention_shared_prefix — decode attention for a batch whose
+ * sequences all begin with the same prefix, held once in the pool: "a hash
+ * table from content hash -> block ID for prefix caching (sharing common
+ * prefixes)" with "reference counting for block sharing" (Nano-vLLM System
+ * Architecture Analysis, §2 Core Components, "Paged KV Cache").
+ *
+ * Results are those of paged_decode_attention on the same arguments.  The
+ * first shared_prefix_tokens tokens (a multiple of block_size, at most
+ * max_blocks_per_seq*block_size) of every sequence must be the same physical
+ * blocks: entries [0, shared_prefix_tokens/block_size) of every row of
+ * block_tables equal those of row 0, and every context_lens[b] >=
+ * shared_prefix_tokens.  The call computes attention over those shared keys
+ * once for all B*Hq query rows, as a dense tcgen05 tile product per kv head
+ * (query rows = the group's (sequence, head) pairs), then runs the split decode
+ * over each sequence's own tokens [shared_prefix_tokens, ctx) and folds the
+ * shared part into the log-sum-exp merge.  The shared blocks are read once per
+ * kv head instead of once per sequence.
+ * workspace: at least paged_decode_shared_prefix_workspace_bytes(...) bytes,
+ * with the conventions of paged_decode_attention (first MiB zero before first
+ * use; left zero by every call).  Two kernels run on `stream`.
+ * shared_prefix_tokens == 0 is exactly paged_decode_attention.  A table row
+ * whose prefix entries differ from row 0's, or a context shorter than the
+ * prefix, is reported as PKV_ERR_DEVICE_INDEX through pkv_get_device_error().
+ * Returns PKV_OK, PKV_ERR_ARG (also for a prefix that is not whole blocks or
+ * is longer than the tables), PKV_ERR_SHAPE, PKV_ERR_WORKSPACE or
+ * PKV_ERR_LAUNCH. */
+int paged_decode_attention_shared_prefix(void* out, float* lse, const void* q,
+                                         const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables,
+                                         int max_blocks_per_seq,
+                                         const int32_t* context_lens, int B, int Hq,
+                                         int Hkv, int D, int block_size, int64_t num_blocks,
+                                         float scale, int shared_prefix_tokens,
+                                         void* workspace, size_t workspace_bytes,
+                                         int num_splits, pkv_stream_t stream);
+
 /* Size of the fixed device scratch array behind
  * paged_decode_attention_noalloc (16 MiB per device that loads the library). */
 #define PKV_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)

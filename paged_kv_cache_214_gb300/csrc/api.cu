@@ -126,7 +126,7 @@ extern "C" size_t paged_decode_workspace_bytes(int B, int Hq, int Hkv, int D,
                                                int num_splits) {
   if (D != kHeadDim || block_size != kBlockSize || num_splits < 0) return 0;
   DecodePlan plan;
-  if (plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), &plan))
+  if (plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), 0, &plan))
     return 0;
   return plan.workspace_bytes;
 }
@@ -136,7 +136,7 @@ extern "C" int paged_decode_num_splits(int B, int Hq, int Hkv, int D, int max_bl
   if (D != kHeadDim || block_size != kBlockSize) return PKV_ERR_SHAPE;
   if (num_splits < 0) return PKV_ERR_ARG;
   DecodePlan plan;
-  const int st = plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), &plan);
+  const int st = plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), 0, &plan);
   return st ? st : plan.num_splits;
 }
 
@@ -157,7 +157,7 @@ extern "C" int paged_decode_attention(void* out, float* lse, const void* q, cons
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PKV_ERR_ARG;
   DecodePlan plan;
-  st = plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), &plan);
+  st = plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), 0, &plan);
   if (st) return st;
   if (plan.workspace_bytes) {
     if (!workspace || workspace_bytes < plan.workspace_bytes ||
@@ -167,8 +167,77 @@ extern "C" int paged_decode_attention(void* out, float* lse, const void* q, cons
   unsigned* err = device_error_word();
   if (!err) return PKV_ERR_LAUNCH;
   DecodeArgs a{out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-               B, Hq, Hkv, num_blocks, scale, workspace, workspace_bytes, num_splits};
+               B, Hq, Hkv, num_blocks, scale, workspace, workspace_bytes, num_splits, 0};
   return launch_decode(a, plan, err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+namespace {
+
+int check_shared_prefix(int max_blocks_per_seq, int shared_prefix_tokens) {
+  if (shared_prefix_tokens < 0 || shared_prefix_tokens % kBlockSize) return PKV_ERR_ARG;
+  if (shared_prefix_tokens / kBlockSize > max_blocks_per_seq) return PKV_ERR_ARG;
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" size_t paged_decode_shared_prefix_workspace_bytes(int B, int Hq, int Hkv, int D,
+                                                             int max_blocks_per_seq,
+                                                             int block_size,
+                                                             int shared_prefix_tokens,
+                                                             int num_splits) {
+  if (D != kHeadDim || block_size != kBlockSize || num_splits < 0) return 0;
+  if (check_shared_prefix(max_blocks_per_seq, shared_prefix_tokens)) return 0;
+  DecodePlan plan;
+  if (plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(),
+                  shared_prefix_tokens / kBlockSize, &plan))
+    return 0;
+  return plan.workspace_bytes;
+}
+
+extern "C" int paged_decode_attention_shared_prefix(
+    void* out, float* lse, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens, int B,
+    int Hq, int Hkv, int D, int block_size, int64_t num_blocks, float scale,
+    int shared_prefix_tokens, void* workspace, size_t workspace_bytes, int num_splits,
+    pkv_stream_t stream) {
+  int st = check_shared_prefix(max_blocks_per_seq, shared_prefix_tokens);
+  if (st) return st;
+  if (shared_prefix_tokens == 0)
+    return paged_decode_attention(out, lse, q, k_cache, v_cache, block_tables,
+                                  max_blocks_per_seq, context_lens, B, Hq, Hkv, D, block_size,
+                                  num_blocks, scale, workspace, workspace_bytes, num_splits,
+                                  stream);
+  if (B < 0 || Hq <= 0 || max_blocks_per_seq < 0 || num_splits < 0) return PKV_ERR_ARG;
+  st = check_pool(Hkv, D, block_size, num_blocks);
+  if (st) return st;
+  if (Hq % Hkv) return PKV_ERR_SHAPE;
+  if (B == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !context_lens || !block_tables) return PKV_ERR_ARG;
+  if (num_blocks == 0) return PKV_ERR_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_ARG;
+  DecodePlan plan;
+  st = plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(),
+                   shared_prefix_tokens / kBlockSize, &plan);
+  if (st) return st;
+  if (!workspace || workspace_bytes < plan.workspace_bytes ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return PKV_ERR_WORKSPACE;
+  unsigned* err = device_error_word();
+  if (!err) return PKV_ERR_LAUNCH;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* pbase = static_cast<uint8_t*>(workspace) + plan.prefix_offset;
+  const size_t o_bytes = (static_cast<size_t>(B) * Hq * kHeadDim * sizeof(float) + 255) / 256 * 256;
+  PrefixArgs pa{reinterpret_cast<float*>(pbase), reinterpret_cast<float*>(pbase + o_bytes), q,
+                k_cache, v_cache, block_tables, B, Hq, Hkv, shared_prefix_tokens, num_blocks,
+                scale};
+  st = launch_prefix_attention(pa, err, cs);
+  if (st) return st;
+  DecodeArgs a{out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+               B, Hq, Hkv, num_blocks, scale, workspace, workspace_bytes, num_splits,
+               shared_prefix_tokens};
+  return launch_decode(a, plan, err, cs);
 }
 
 extern "C" int paged_prefill_attention(void* out, float* lse, const void* q, const void* k_cache,

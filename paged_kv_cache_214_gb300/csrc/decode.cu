@@ -72,6 +72,13 @@ struct DecodeParams {
   int B, Hq, Hkv, maxblk, num_splits, split_blocks, head_groups;
   int64_t num_blocks;
   float scale_log2;
+  // Shared prefix (0 = none): every sequence's first prefix_tokens tokens are
+  // the same physical blocks, already reduced to one normalised partial per
+  // (sequence, query head); this kernel then covers [prefix_tokens, ctx) only
+  // and folds that partial into its merge.
+  int prefix_tokens;
+  const float* prefix_o;    // [B*Hq, 128]
+  const float* prefix_lse;  // [B*Hq] log2-sum-exp
 };
 
 template <int G>
@@ -118,57 +125,49 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
+  // Block ids of this split's whole range, loaded speculatively (they do not
+  // depend on the context length, so both loads are in flight together).
+  const int split_tokens = p.split_blocks * kBlockSize;
+  const int blk_begin = (p.prefix_tokens + split * split_tokens) / kBlockSize;
+  int spec_id = 0;
+  if (warp == 0 && lane < p.split_blocks && blk_begin + lane < p.maxblk)
+    spec_id = __ldg(p.block_tables + static_cast<int64_t>(b) * p.maxblk + blk_begin + lane);
   // Context of this sequence (clamped to what its block table can address).
   int ctx = p.context_lens[b];
   const int cap = p.maxblk * kBlockSize;
-  if (ctx < 0 || ctx > cap) {
+  const int P = p.prefix_tokens;
+  if (ctx < 0 || ctx > cap || ctx < P) {
     if (tid == 0 && split == 0 && hg == 0) record_error(p.err, kErrIndex);
-    ctx = ctx < 0 ? 0 : cap;
+    ctx = ctx < P ? P : cap;
   }
-  const int split_tokens = p.split_blocks * kBlockSize;
-  const int nsplit = (ctx + split_tokens - 1) / split_tokens;
+  const int nsplit = (ctx - P + split_tokens - 1) / split_tokens;
   if (split >= (nsplit > 0 ? nsplit : 1)) return;  // whole block exits: no work
 
-  if (ctx == 0) {  // empty context: out = 0, lse = -inf
+  if (P > 0 && split == 0 && hg == 0 && warp == 0) {
+    // the shared prefix must be the same physical blocks as sequence 0's
+    const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.maxblk;
+    bool same = true;
+    for (int i = lane; i < P / kBlockSize; i += 32) same &= row[i] == p.block_tables[i];
+    if (!__all_sync(0xffffffffu, same) && lane == 0) record_error(p.err, kErrIndex);
+  }
+
+  if (ctx == P) {  // nothing past the prefix: out = the prefix's result (or 0, -inf)
     for (int i = tid; i < G * kHeadDim; i += kThreads) {
       const int h = i / kHeadDim, d = i % kHeadDim;
-      p.out[(static_cast<int64_t>(b) * p.Hq + h0 + h) * kHeadDim + d] = __float2bfloat16_rn(0.f);
+      const int64_t row = static_cast<int64_t>(b) * p.Hq + h0 + h;
+      p.out[row * kHeadDim + d] =
+          __float2bfloat16_rn(P > 0 ? __ldcg(p.prefix_o + row * kHeadDim + d) : 0.f);
     }
-    if (p.lse && tid < G) p.lse[static_cast<int64_t>(b) * p.Hq + h0 + tid] = -INFINITY;
+    if (p.lse && tid < G) {
+      const int64_t row = static_cast<int64_t>(b) * p.Hq + h0 + tid;
+      p.lse[row] = P > 0 ? __ldcg(p.prefix_lse + row) * kLn2 : -INFINITY;
+    }
     return;
   }
 
-  const int tok_begin = split * split_tokens;
+  const int tok_begin = P + split * split_tokens;
   const int tok_end = min(ctx, tok_begin + split_tokens);
   const int n_tiles = (tok_end - tok_begin + kTile - 1) / kTile;
-  const int blk_begin = split * p.split_blocks;
-
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), kConsumerWarps);
-    }
-    flags[0] = 0;  // abort
-    flags[1] = 0;  // last-arrival flag
-    flags[2] = 0;  // tiles issued
-    fence_barrier_init();
-    tma_prefetch_map(&kmap);
-    tma_prefetch_map(&vmap);
-  }
-  if (warp == 0) {
-    // Block ids of this range (validated; a bad id is reported and replaced by
-    // block 0 so that no out-of-range address is ever formed).
-    const int nblk = (tok_end - 1) / kBlockSize - blk_begin + 1;
-    if (lane < nblk) {
-      int id = p.block_tables[static_cast<int64_t>(b) * p.maxblk + blk_begin + lane];
-      if (id < 0 || id >= p.num_blocks) {
-        record_error(p.err, kErrIndex);
-        id = 0;
-      }
-      sblk[lane] = id;
-    }
-  }
-  __syncthreads();
 
   // Lane 0 of warp 0 is the producer: it fills the ring up front and refills a
   // stage as soon as all four warps have released it.
@@ -186,9 +185,33 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     tma_load_3d_hint(vdst + kHalfBytes, &vmap, full_bar(s), 64, kvh, slot, policy);
     flags[2] = it + 1;
   };
-  if (tid == 0) {
-    for (int it = 0; it < kStages && it < n_tiles; ++it) issue(it);
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(full_bar(s), 1);
+        mbar_init(empty_bar(s), kConsumerWarps);
+      }
+      flags[0] = 0;  // abort
+      flags[1] = 0;  // last-arrival flag
+      flags[2] = 0;  // tiles issued
+      fence_barrier_init();
+    }
+    // Block ids of the range actually used (validated; a bad id is reported
+    // and replaced by block 0 so that no out-of-range address is ever formed).
+    const int nblk = (tok_end - 1) / kBlockSize - blk_begin + 1;
+    if (lane < nblk) {
+      if (spec_id < 0 || spec_id >= p.num_blocks) {
+        record_error(p.err, kErrIndex);
+        spec_id = 0;
+      }
+      sblk[lane] = spec_id;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      for (int it = 0; it < kStages && it < n_tiles; ++it) issue(it);
+    }
   }
+  __syncthreads();
 
   {
     // ------------------------------------------------------------ consumers
@@ -371,7 +394,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   // ---------------------------------------------------------------- epilogue
   // thread tid (0..127) owns dim d = tid of every head
   const int d = tid;
-  const bool single = nsplit == 1;
+  const bool single = nsplit == 1 && P == 0;
   for (int h = 0; h < G; ++h) {
     float M = -INFINITY;
 #pragma unroll
@@ -398,21 +421,26 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   if (single) return;
 
   // ---------------------------------------------------------------- split merge
-  __threadfence();
+  // All partial stores of the block precede the barrier; one thread then
+  // publishes them at device scope and takes the ticket.
   named_barrier(1, kConsumerWarps * 32);
   unsigned* counter = p.ws_count + static_cast<int64_t>(b) * p.Hkv * p.head_groups + hg;
   if (tid == 0) {
+    __threadfence();
     const unsigned ticket = atomicAdd(counter, 1u);
-    flags[1] = (ticket == static_cast<unsigned>(nsplit - 1)) ? 1 : 0;
+    const bool last = ticket == static_cast<unsigned>(nsplit - 1);
+    if (last) __threadfence();
+    flags[1] = last ? 1 : 0;
   }
   named_barrier(1, kConsumerWarps * 32);
   if (!flags[1]) return;
-  __threadfence();
   for (int h = warp; h < G; h += kConsumerWarps) {
     const int64_t row = static_cast<int64_t>(b) * p.Hq + h0 + h;
     const float* lrow = p.ws_lse + row * p.num_splits;
-    // lanes over splits: max and sum of 2^(lse_s - max) by warp shuffles
-    float mx = -INFINITY;
+    // lanes over splits: max and sum of 2^(lse_s - max) by warp shuffles; the
+    // shared prefix's partial, if any, is one more term
+    const float lp = P > 0 ? __ldcg(p.prefix_lse + row) : -INFINITY;
+    float mx = lp;
     for (int s = lane; s < nsplit; s += 32) mx = fmaxf(mx, __ldcg(lrow + s));
 #pragma unroll
     for (int sh = 16; sh >= 1; sh >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
@@ -420,9 +448,15 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     for (int s = lane; s < nsplit; s += 32) sum += rescale(__ldcg(lrow + s), mx);
 #pragma unroll
     for (int sh = 16; sh >= 1; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
+    sum += rescale(lp, mx);
     const float inv = 1.f / sum;
     // lanes over dims (4 each): out = sum_s w_s * o_s
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (P > 0) {
+      const float w = rescale(lp, mx) * inv;
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(p.prefix_o + row * kHeadDim) + lane);
+      acc = make_float4(w * v.x, w * v.y, w * v.z, w * v.w);
+    }
     for (int s = 0; s < nsplit; ++s) {
       const float w = rescale(__ldcg(lrow + s), mx) * inv;
       const float4 v = __ldcg(reinterpret_cast<const float4*>(
@@ -467,14 +501,17 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 }  // namespace
 
 int plan_decode(int B, int Hq, int Hkv, int max_blocks_per_seq, int num_splits,
-                int sm_count, DecodePlan* plan) {
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || max_blocks_per_seq < 0) return PKV_ERR_ARG;
+                int sm_count, int prefix_blocks, DecodePlan* plan) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || max_blocks_per_seq < 0 || prefix_blocks < 0 ||
+      prefix_blocks > max_blocks_per_seq)
+    return PKV_ERR_ARG;
   if (Hq % Hkv) return PKV_ERR_SHAPE;
   const int g = Hq / Hkv;
   const int G = (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1;
   plan->heads_per_cta = G;
   plan->head_groups = g / G;
-  const int maxblk = max_blocks_per_seq > 0 ? max_blocks_per_seq : 1;
+  const int rest = max_blocks_per_seq - prefix_blocks;
+  const int maxblk = rest > 0 ? rest : 1;
   int split_blocks;
   if (num_splits > 0) {
     split_blocks = (maxblk + num_splits - 1) / num_splits;
@@ -494,7 +531,8 @@ int plan_decode(int B, int Hq, int Hkv, int max_blocks_per_seq, int num_splits,
   split_blocks = (maxblk + S - 1) / S;
   plan->split_blocks = split_blocks;
   plan->num_splits = S;
-  if (S == 1) {
+  plan->prefix_offset = 0;
+  if (S == 1 && prefix_blocks == 0) {
     plan->workspace_bytes = 0;
   } else {
     if (static_cast<int64_t>(B) * Hkv * plan->head_groups > kMaxCounters) return PKV_ERR_SHAPE;
@@ -502,6 +540,12 @@ int plan_decode(int B, int Hq, int Hkv, int max_blocks_per_seq, int num_splits,
     size_t bytes = kCounterRegion;
     bytes += align_up(rows * kHeadDim * sizeof(float), 256);
     bytes += align_up(rows * sizeof(float), 256);
+    if (prefix_blocks > 0) {
+      plan->prefix_offset = bytes;
+      const size_t prow = static_cast<size_t>(B) * Hq;
+      bytes += align_up(prow * kHeadDim * sizeof(float), 256);
+      bytes += align_up(prow * sizeof(float), 256);
+    }
     plan->workspace_bytes = bytes;
   }
   return PKV_OK;
@@ -531,7 +575,16 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
   prm.head_groups = plan.head_groups;
   prm.num_blocks = a.num_blocks;
   prm.scale_log2 = a.scale * 1.4426950408889634f;
-  if (plan.num_splits > 1) {
+  prm.prefix_tokens = a.prefix_tokens;
+  prm.prefix_o = nullptr;
+  prm.prefix_lse = nullptr;
+  if (a.prefix_tokens > 0) {
+    const uint8_t* base = static_cast<const uint8_t*>(a.workspace) + plan.prefix_offset;
+    prm.prefix_o = reinterpret_cast<const float*>(base);
+    prm.prefix_lse = reinterpret_cast<const float*>(
+        base + align_up(static_cast<size_t>(a.B) * a.Hq * kHeadDim * sizeof(float), 256));
+  }
+  if (plan.workspace_bytes > 0) {
     const size_t rows = static_cast<size_t>(a.B) * a.Hq * plan.num_splits;
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     prm.ws_count = reinterpret_cast<unsigned*>(ws);

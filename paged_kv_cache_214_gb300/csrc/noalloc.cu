@@ -65,7 +65,7 @@ extern "C" int paged_decode_attention_noalloc(void* out, float* lse, const void*
   if (B < 0 || Hq <= 0 || Hkv <= 0 || max_blocks_per_seq < 0 || num_splits < 0)
     return PKV_ERR_ARG;
   DecodePlan plan;
-  int st = plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), &plan);
+  int st = plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), 0, &plan);
   if (st) return st;
   // This call's partials and counters must fit the fixed scratch array.
   if (plan.workspace_bytes > kNoAllocScratchBytes) return PKV_ERR_WORKSPACE;

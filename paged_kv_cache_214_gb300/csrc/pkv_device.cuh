@@ -134,6 +134,14 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// ex2 kept in program order with the other volatile statements (tensor-memory
+// loads), so that a loop over TMEM chunks holds one chunk in registers at a time.
+__device__ __forceinline__ float ex2_ordered(float x) {
+  float y;
+  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Two bf16 packed in a 32-bit word -> two floats (exact: bf16 is the top half
 // of a binary32).
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }

@@ -58,6 +58,7 @@ struct DecodeArgs {
   void* workspace;
   size_t workspace_bytes;
   int num_splits;  // as requested (0 = automatic)
+  int prefix_tokens;  // shared prefix handled by a separate pass (0 = none)
 };
 
 // Split plan of one decode call.
@@ -66,11 +67,30 @@ struct DecodePlan {
   int head_groups;    // (Hq/Hkv) / G
   int split_blocks;   // whole KV blocks per split
   int num_splits;     // S
+  size_t prefix_offset;  // byte offset of the shared-prefix partials (if any)
   size_t workspace_bytes;
 };
-// Returns PKV_OK and fills `plan`, or a negative status.
+// Returns PKV_OK and fills `plan`, or a negative status.  prefix_blocks: blocks
+// of a shared prefix reduced separately (the splits cover the rest).
 int plan_decode(int B, int Hq, int Hkv, int max_blocks_per_seq, int num_splits,
-                int sm_count, DecodePlan* plan);
+                int sm_count, int prefix_blocks, DecodePlan* plan);
+
+// Attention of every (sequence, query head) of the batch over a shared prefix
+// of prefix_tokens tokens (the first blocks of sequence 0's table), as one
+// normalised fp32 partial [B*Hq, 128] plus log2-sum-exp [B*Hq] per row.
+struct PrefixArgs {
+  float* part_o;
+  float* part_lse;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  int B, Hq, Hkv;
+  int prefix_tokens;
+  int64_t num_blocks;
+  float scale;
+};
+int launch_prefix_attention(const PrefixArgs& a, unsigned* err, cudaStream_t stream);
 int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
                   cudaStream_t stream);
 

@@ -349,22 +349,22 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
       // S_x(kt) is complete, and so is every earlier MMA (PV_x(kt-1) included)
       if (!(ok = warp_wait(bar(kBarSFull + x), kt & 1))) break;
       tc_fence_after();
-      // pass 1: row max of the raw scores (the scale is positive, so it is
-      // applied to the max afterwards)
+      // Pass 1: row max of the raw scores, 64 columns per TMEM round trip (the
+      // scale is positive, so it is applied to the max afterwards).
       const int j0 = kt * kN;
       const bool edge = !kPrefix && j0 + kN - 1 > my_diag;   // causal edge inside this tile
-      float mt = -INFINITY;
+      float smax = -INFINITY;
 #pragma unroll 1
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t r[32];
-        tmem_ld32_wait(s_col + c4 * 32, r);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t r[64];
+        tmem_ld64_wait(s_col + hh * 64, r);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
+        for (int c = 0; c < 64; ++c) {
           const float v = __uint_as_float(r[c]);
-          mt = fmaxf(mt, (!edge || j0 + c4 * 32 + c <= vis) ? v : -INFINITY);
+          smax = fmaxf(smax, (!edge || j0 + hh * 64 + c <= vis) ? v : -INFINITY);
         }
       }
-      mt *= p.scale_log2;
+      const float mt = smax * p.scale_log2;
       if (kt == 0) {
         m = mt;  // key 0 is visible to every row
       } else {
@@ -375,29 +375,29 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
             l *= alpha;
             m = mt;
           }
-#pragma unroll
+#pragma unroll 1
           for (int c4 = 0; c4 < 4; ++c4) {
-            uint32_t r[32];
-            tmem_ld32_wait(o_col + c4 * 32, r);
+            uint32_t o[32];
+            tmem_ld32_wait(o_col + c4 * 32, o);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
-            tmem_st32(o_col + c4 * 32, r);
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st32(o_col + c4 * 32, o);
           }
         }
       }
-      // pass 2: P = 2^(scale*s - m) as bf16 pairs over the first 64 columns of
-      // S_x: score columns [32c, 32c+32) become P columns [16c, 16c+16), all of
-      // which have been read already
+      // Pass 2: P = 2^(scale*s - m) as bf16 pairs over the first 64 columns of
+      // S_x: score columns [64hh, 64hh+64) become P columns [32hh, 32hh+32),
+      // all of which have been read already.
       const float neg_m = -m;
       float rs = 0.f;
 #pragma unroll 1
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t r[32];
-        tmem_ld32_wait(s_col + c4 * 32, r);
-        uint32_t pk[16];
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t r[64];
+        tmem_ld64_wait(s_col + hh * 64, r);
+        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int k0 = j0 + c4 * 32 + 2 * c;
+        for (int c = 0; c < 32; ++c) {
+          const int k0 = j0 + hh * 64 + 2 * c;
           float e0 = ex2(fmaf(__uint_as_float(r[2 * c]), p.scale_log2, neg_m));
           float e1 = ex2(fmaf(__uint_as_float(r[2 * c + 1]), p.scale_log2, neg_m));
           if (edge) {
@@ -407,7 +407,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
           rs += e0 + e1;
           pk[c] = pack_bf16x2(e0, e1);
         }
-        tmem_st16(s_col + c4 * 16, pk);
+        tmem_st32(s_col + hh * 32, pk);
       }
       l += rs;
       tmem_wait_st();

@@ -60,6 +60,12 @@ def load_library(path: str = LIB_PATH):
         lib.paged_decode_attention.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32,
                                                i32, i64, f32, P, sz, i32, P]
         lib.paged_decode_attention.restype = i32
+        lib.paged_decode_shared_prefix_workspace_bytes.argtypes = [i32] * 8
+        lib.paged_decode_shared_prefix_workspace_bytes.restype = sz
+        lib.paged_decode_attention_shared_prefix.argtypes = [P, P, P, P, P, P, i32, P, i32, i32,
+                                                             i32, i32, i32, i64, f32, i32, P,
+                                                             sz, i32, P]
+        lib.paged_decode_attention_shared_prefix.restype = i32
         lib.paged_decode_attention_noalloc.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32,
                                                        i32, i32, i64, f32, i32, P]
         lib.paged_decode_attention_noalloc.restype = i32
@@ -201,6 +207,55 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                                       _ptr(context_lens), B, Hq, Hkv, D, bs, NB, float(scale),
                                       _ptr(workspace), ws_bytes, int(num_splits),
                                       _stream(stream)), "paged_decode_attention")
+    return out, lse
+
+
+def paged_decode_shared_prefix_workspace_bytes(B: int, Hq: int, Hkv: int, D: int,
+                                               max_blocks_per_seq: int,
+                                               shared_prefix_tokens: int,
+                                               block_size: int = 256,
+                                               num_splits: int = 0) -> int:
+    return int(load_library().paged_decode_shared_prefix_workspace_bytes(
+        B, Hq, Hkv, D, max_blocks_per_seq, block_size, shared_prefix_tokens, num_splits))
+
+
+def paged_decode_attention_shared_prefix(q: torch.Tensor, k_cache: torch.Tensor,
+                                         v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                         context_lens: torch.Tensor, scale: float,
+                                         shared_prefix_tokens: int,
+                                         out: Optional[torch.Tensor] = None,
+                                         lse: Optional[torch.Tensor] = None,
+                                         workspace: Optional[torch.Tensor] = None,
+                                         num_splits: int = 0, want_lse: bool = True,
+                                         stream=None
+                                         ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Decode for a batch whose sequences all start with the same
+    `shared_prefix_tokens` tokens (the same physical blocks at the start of every
+    table row).  Same results as paged_decode_attention."""
+    lib = load_library()
+    NB, bs, Hkv, D = _pool_dims(k_cache, v_cache)
+    _need(q, "q", torch.bfloat16, 3)
+    B, Hq, _ = q.shape
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    maxblk = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    need = paged_decode_shared_prefix_workspace_bytes(B, Hq, Hkv, D, maxblk,
+                                                      shared_prefix_tokens, bs, num_splits)
+    if workspace is None and need:
+        workspace = decode_workspace(need, q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.paged_decode_attention_shared_prefix(
+        _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), maxblk,
+        _ptr(context_lens), B, Hq, Hkv, D, bs, NB, float(scale), int(shared_prefix_tokens),
+        _ptr(workspace), ws_bytes, int(num_splits), _stream(stream)),
+        "paged_decode_attention_shared_prefix")
     return out, lse
 
 

@@ -172,8 +172,10 @@ def make_decode(context_lens: Sequence[int], Hq: int, Hkv: int, num_blocks: int,
         raise ValueError("shared prefix must be whole blocks")
     n_shared = shared_prefix_tokens // block_size
     for L in lens:
-        if shared_prefix_tokens and L <= shared_prefix_tokens:
-            raise ValueError("with a shared prefix every context must extend past it")
+        if shared_prefix_tokens and (L < shared_prefix_tokens or
+                                     (store_new_token and L == shared_prefix_tokens)):
+            raise ValueError("with a shared prefix every context must cover it, and a new "
+                             "token must land past it")
     gen = torch.Generator().manual_seed(seed)
     nblk = [_cdiv(L, block_size) for L in lens]
     maxblk = max_blocks_per_seq or max([1] + nblk)
