@@ -664,6 +664,38 @@ def run_prefill_profile(args):
                       "TFLOP/s": round(fl / (med / 1e3) / 1e12, 1)}), flush=True)
 
 
+def run_shared_prefix_profile(args):
+    """Small-footprint shared-prefix decode run for ncu: the
+    prefix-shared-decode-b256 batch with the pool trimmed to the blocks it
+    uses."""
+    from paged_kv_cache_214_gb300 import pkv
+    dev = torch.device("cuda", torch.cuda.current_device())
+    s = W.seed_for(3)
+    lens = [2048 + x + 1 for x in W._uniform_ints(0, 6144, 256, s)]
+    nblk = 8 + sum(-(-L // W.BLOCK_SIZE) - 8 for L in lens)
+    w = W.make_decode(lens, 32, 8, nblk, s, name="prefix-shared-decode-b256",
+                      shared_prefix_tokens=2048, store_new_token=False, pool_device=dev)
+    q, tables, ctx = w.q.to(dev), w.block_tables.to(dev), w.context_lens.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    need = pkv.paged_decode_shared_prefix_workspace_bytes(w.B, w.Hq, w.Hkv, w.D,
+                                                          tables.shape[1], 2048)
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        pkv.paged_decode_attention_shared_prefix(q, w.k_cache, w.v_cache, tables, ctx, w.scale,
+                                                 2048, out=out, lse=lse, workspace=ws,
+                                                 stream=stream)
+    for _ in range(args.warmup):
+        call()
+    med, _ = _time_calls(call, args.steps, stream)
+    assert pkv.get_device_error() == pkv.PKV_OK
+    ub = decode_bytes(w, unique=True) / (med / 1e3) / 1e9
+    print(json.dumps({"workload": w.name, "us": round(med * 1e3, 2),
+                      "unique_GB/s": round(ub, 1)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -672,7 +704,8 @@ def main():
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-kernel", choices=["decode", "prefill"], default="decode",
+    ap.add_argument("--profile-kernel", choices=["decode", "prefill", "shared-prefix"],
+                    default="decode",
                     help="with --profile: which kernel the run exercises")
     ap.add_argument("--profile", action="store_true",
                     help="small-footprint run for ncu: one batch, trimmed pool, "
@@ -686,6 +719,9 @@ def main():
     world, rank, local = dist_setup(args)
     if args.profile_kernel == "prefill":
         run_prefill_profile(args)
+        return
+    if args.profile_kernel == "shared-prefix":
+        run_shared_prefix_profile(args)
         return
     if args.impl == "reference":
         res = run_reference(args, world, rank)

@@ -76,6 +76,23 @@ int kv_cache_store(const void* k, const void* v, int64_t k_tok_stride,
                    const int32_t* slot_mapping, int64_t T, int Hkv, int D,
                    int block_size, int64_t num_blocks, pkv_stream_t stream);
 
+/* kv_cache_copy_blocks — the device half of copy-on-write block sharing
+ * ("reference counting for block sharing (copy-on-write semantics)", Nano-vLLM
+ * System Architecture Analysis, §2 Core Components, "Paged KV Cache"): for
+ * i in [0, n_pairs), block dst_blocks[i] of k_cache and of v_cache becomes a
+ * bit copy of block src_blocks[i] (whole blocks: block_size x Hkv x D).  The
+ * host block manager (pkv_blocks.h) reports these pairs when a sequence
+ * appends to a shared, partly filled block.
+ * src_blocks, dst_blocks: int32 [n_pairs] on the device.  Destination blocks
+ * must be distinct and must not be any pair's source; otherwise the result is
+ * unspecified.  A block id outside [0, num_blocks) skips that pair and is
+ * reported as PKV_ERR_DEVICE_INDEX through pkv_get_device_error().
+ * Returns PKV_OK, PKV_ERR_ARG, PKV_ERR_SHAPE or PKV_ERR_LAUNCH; n_pairs == 0 is
+ * a no-op. */
+int kv_cache_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_blocks,
+                         const int32_t* dst_blocks, int n_pairs, int Hkv, int D,
+                         int block_size, int64_t num_blocks, pkv_stream_t stream);
+
 /* paged_decode_workspace_bytes — bytes of device workspace that a
  * paged_decode_attention call with the same (B, Hq, Hkv, D, max_blocks_per_seq,
  * block_size, num_splits) needs.  0 means the call needs none (a single split).

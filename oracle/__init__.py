@@ -73,8 +73,9 @@ def _declare(lib):
                                   i32, i64, f64, i32]
     lib.oracle_prefill.argtypes = [P, P, P, P, P, P, i32, P, P, i32, i32, i32,
                                    i32, i32, i64, f64, i32]
+    lib.oracle_copy_blocks.argtypes = [P, P, P, P, i64, i32, i32, i32, i64]
     for fn in ("oracle_store", "oracle_gather", "oracle_decode", "oracle_prefill",
-               "oracle_hardware_threads"):
+               "oracle_hardware_threads", "oracle_copy_blocks"):
         getattr(lib, fn).restype = ctypes.c_int
     return lib
 
@@ -129,6 +130,17 @@ def store(k, v, k_cache, v_cache, slot_mapping, lib=None) -> None:
     sm = _i32(slot_mapping)
     _check(lib.oracle_store(_ptr(k), _ptr(v), Hkv * D, Hkv * D, _ptr(k_cache),
                             _ptr(v_cache), _ptr(sm), T, Hkv, D, bs, NB))
+
+
+def copy_blocks(k_cache, v_cache, src, dst, lib=None) -> None:
+    """In-place: block dst[i] of both caches [NB, bs, Hkv, D] := block src[i]."""
+    lib = lib or load()
+    if k_cache.dtype != np.uint16 or not k_cache.flags.c_contiguous:
+        raise TypeError("caches must be C-contiguous uint16")
+    NB, bs, Hkv, D = k_cache.shape
+    s, d = _i32(src), _i32(dst)
+    _check(lib.oracle_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(s), _ptr(d), len(s), Hkv,
+                                  D, bs, NB))
 
 
 def gather(k_cache, v_cache, table_row, L, lib=None):

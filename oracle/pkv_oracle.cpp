@@ -176,6 +176,25 @@ int oracle_store(const uint16_t* k, const uint16_t* v, int64_t k_tok_stride,
   return 0;
 }
 
+// Copy-on-write block copies ("Reference counting for block sharing
+// (copy-on-write semantics)", same page, §2 "Paged KV Cache"): for each pair,
+// block dst[i] of both caches becomes a copy of block src[i].  Bit copy.
+int oracle_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, const int32_t* src,
+                       const int32_t* dst, int64_t n_pairs, int Hkv, int D,
+                       int block_size, int64_t num_blocks) {
+  if (n_pairs < 0 || Hkv <= 0 || D <= 0 || block_size <= 0) return -1;
+  for (int64_t i = 0; i < n_pairs; ++i)
+    if (src[i] < 0 || dst[i] < 0 || src[i] >= num_blocks || dst[i] >= num_blocks) return -4;
+  const int64_t block_elems = static_cast<int64_t>(block_size) * Hkv * D;
+  for (int64_t i = 0; i < n_pairs; ++i) {
+    std::memcpy(k_cache + dst[i] * block_elems, k_cache + src[i] * block_elems,
+                sizeof(uint16_t) * block_elems);
+    std::memcpy(v_cache + dst[i] * block_elems, v_cache + src[i] * block_elems,
+                sizeof(uint16_t) * block_elems);
+  }
+  return 0;
+}
+
 // Gather of one sequence into contiguous [L, Hkv, D] K and V (bf16 bits).
 // Exposed for the round-trip tests of the addressing.
 int oracle_gather(const uint16_t* k_cache, const uint16_t* v_cache,

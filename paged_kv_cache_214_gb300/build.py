@@ -20,7 +20,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libpkv.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
-SOURCES = ["api.cu", "store.cu", "decode.cu", "prefill.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "store.cu", "decode.cu", "prefill.cu", "noalloc.cu", "blocks.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
               "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]
@@ -51,7 +51,7 @@ def _stale() -> bool:
         return True
     t = os.path.getmtime(LIB)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    deps.append(os.path.join(ROOT, "include", "pkv.h"))
+    deps += [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))]
     return any(os.path.getmtime(d) > t for d in deps)
 
 

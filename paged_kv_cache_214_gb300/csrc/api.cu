@@ -121,6 +121,22 @@ extern "C" int kv_cache_store(const void* k, const void* v, int64_t k_tok_stride
   return launch_store(a, err, reinterpret_cast<cudaStream_t>(stream));
 }
 
+extern "C" int kv_cache_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_blocks,
+                                    const int32_t* dst_blocks, int n_pairs, int Hkv, int D,
+                                    int block_size, int64_t num_blocks, pkv_stream_t stream) {
+  if (n_pairs < 0) return PKV_ERR_ARG;
+  int st = check_pool(Hkv, D, block_size, num_blocks);
+  if (st) return st;
+  if (n_pairs == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !src_blocks || !dst_blocks) return PKV_ERR_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ARG;
+  unsigned* err = device_error_word();
+  if (!err) return PKV_ERR_LAUNCH;
+  const int64_t block_bytes = static_cast<int64_t>(block_size) * Hkv * D * 2;
+  return launch_copy_blocks(k_cache, v_cache, src_blocks, dst_blocks, n_pairs, block_bytes,
+                            num_blocks, err, reinterpret_cast<cudaStream_t>(stream));
+}
+
 extern "C" size_t paged_decode_workspace_bytes(int B, int Hq, int Hkv, int D,
                                                int max_blocks_per_seq, int block_size,
                                                int num_splits) {
@@ -228,10 +244,12 @@ extern "C" int paged_decode_attention_shared_prefix(
   if (!err) return PKV_ERR_LAUNCH;
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* pbase = static_cast<uint8_t*>(workspace) + plan.prefix_offset;
-  const size_t o_bytes = (static_cast<size_t>(B) * Hq * kHeadDim * sizeof(float) + 255) / 256 * 256;
+  const size_t o_bytes =
+      (static_cast<size_t>(B) * Hq * plan.prefix_splits * kHeadDim * sizeof(float) + 255) /
+      256 * 256;
   PrefixArgs pa{reinterpret_cast<float*>(pbase), reinterpret_cast<float*>(pbase + o_bytes), q,
-                k_cache, v_cache, block_tables, B, Hq, Hkv, shared_prefix_tokens, num_blocks,
-                scale};
+                k_cache, v_cache, block_tables, B, Hq, Hkv, shared_prefix_tokens,
+                plan.prefix_splits, plan.prefix_kt_per, num_blocks, scale};
   st = launch_prefix_attention(pa, err, cs);
   if (st) return st;
   DecodeArgs a{out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,

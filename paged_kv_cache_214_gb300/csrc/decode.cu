@@ -77,9 +77,48 @@ struct DecodeParams {
   // (sequence, query head); this kernel then covers [prefix_tokens, ctx) only
   // and folds that partial into its merge.
   int prefix_tokens;
-  const float* prefix_o;    // [B*Hq, 128]
-  const float* prefix_lse;  // [B*Hq] log2-sum-exp
+  int prefix_splits;        // partials per row of the shared-prefix pass
+  const float* prefix_o;    // [B*Hq, prefix_splits, 128]
+  const float* prefix_lse;  // [B*Hq, prefix_splits] log2-sum-exp
 };
+
+// Log-sum-exp merge of one output row by one warp: nsplit partials
+// (lse2[s], o[s][128]) of the row's own tokens plus np partials of a shared
+// prefix, all normalised.  Lanes run over partials for the max and the sum
+// (warp shuffles), then over dims (4 each) for the weighted sum.
+__device__ __forceinline__ void merge_row(const float* lrow, const float* orow, int nsplit,
+                                          const float* plrow, const float* porow, int np,
+                                          __nv_bfloat16* out, float* lse, int lane) {
+  float mx = -INFINITY;
+  for (int s = lane; s < nsplit; s += 32) mx = fmaxf(mx, __ldcg(lrow + s));
+  for (int s = lane; s < np; s += 32) mx = fmaxf(mx, __ldcg(plrow + s));
+#pragma unroll
+  for (int sh = 16; sh >= 1; sh >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
+  float sum = 0.f;
+  for (int s = lane; s < nsplit; s += 32) sum += ex2(__ldcg(lrow + s) - mx);
+  for (int s = lane; s < np; s += 32) sum += ex2(__ldcg(plrow + s) - mx);
+#pragma unroll
+  for (int sh = 16; sh >= 1; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
+  const float inv = 1.f / sum;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto add = [&](const float* o, float l2) {
+    const float w = ex2(l2 - mx) * inv;
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(o) + lane);
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
+  };
+  for (int s = 0; s < np; ++s) add(porow + s * kHeadDim, __ldcg(plrow + s));
+  for (int s = 0; s < nsplit; ++s) add(orow + s * kHeadDim, __ldcg(lrow + s));
+  __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y);
+  __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 packed;
+  packed.x = *reinterpret_cast<uint32_t*>(&lo2);
+  packed.y = *reinterpret_cast<uint32_t*>(&hi2);
+  *reinterpret_cast<uint2*>(out + 4 * lane) = packed;
+  if (lse && lane == 0) *lse = (mx + __log2f(sum)) * 0.69314718055994530942f;
+}
 
 template <int G>
 struct SmemLayout {
@@ -152,16 +191,20 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   }
 
   if (ctx == P) {  // nothing past the prefix: out = the prefix's result (or 0, -inf)
+    if (P > 0) {
+      for (int h = warp; h < G; h += kConsumerWarps) {
+        const int64_t row = static_cast<int64_t>(b) * p.Hq + h0 + h;
+        const int np = p.prefix_splits;
+        merge_row(nullptr, nullptr, 0, p.prefix_lse + row * np, p.prefix_o + row * np * kHeadDim,
+                  np, p.out + row * kHeadDim, p.lse ? p.lse + row : nullptr, lane);
+      }
+      return;
+    }
     for (int i = tid; i < G * kHeadDim; i += kThreads) {
       const int h = i / kHeadDim, d = i % kHeadDim;
-      const int64_t row = static_cast<int64_t>(b) * p.Hq + h0 + h;
-      p.out[row * kHeadDim + d] =
-          __float2bfloat16_rn(P > 0 ? __ldcg(p.prefix_o + row * kHeadDim + d) : 0.f);
+      p.out[(static_cast<int64_t>(b) * p.Hq + h0 + h) * kHeadDim + d] = __float2bfloat16_rn(0.f);
     }
-    if (p.lse && tid < G) {
-      const int64_t row = static_cast<int64_t>(b) * p.Hq + h0 + tid;
-      p.lse[row] = P > 0 ? __ldcg(p.prefix_lse + row) * kLn2 : -INFINITY;
-    }
+    if (p.lse && tid < G) p.lse[static_cast<int64_t>(b) * p.Hq + h0 + tid] = -INFINITY;
     return;
   }
 
@@ -436,43 +479,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   if (!flags[1]) return;
   for (int h = warp; h < G; h += kConsumerWarps) {
     const int64_t row = static_cast<int64_t>(b) * p.Hq + h0 + h;
-    const float* lrow = p.ws_lse + row * p.num_splits;
-    // lanes over splits: max and sum of 2^(lse_s - max) by warp shuffles; the
-    // shared prefix's partial, if any, is one more term
-    const float lp = P > 0 ? __ldcg(p.prefix_lse + row) : -INFINITY;
-    float mx = lp;
-    for (int s = lane; s < nsplit; s += 32) mx = fmaxf(mx, __ldcg(lrow + s));
-#pragma unroll
-    for (int sh = 16; sh >= 1; sh >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
-    float sum = 0.f;
-    for (int s = lane; s < nsplit; s += 32) sum += rescale(__ldcg(lrow + s), mx);
-#pragma unroll
-    for (int sh = 16; sh >= 1; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
-    sum += rescale(lp, mx);
-    const float inv = 1.f / sum;
-    // lanes over dims (4 each): out = sum_s w_s * o_s
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (P > 0) {
-      const float w = rescale(lp, mx) * inv;
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(p.prefix_o + row * kHeadDim) + lane);
-      acc = make_float4(w * v.x, w * v.y, w * v.z, w * v.w);
-    }
-    for (int s = 0; s < nsplit; ++s) {
-      const float w = rescale(__ldcg(lrow + s), mx) * inv;
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(
-          p.ws_o + (row * p.num_splits + s) * kHeadDim) + lane);
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
-    }
-    __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y);
-    __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z, acc.w);
-    uint2 packed;
-    packed.x = *reinterpret_cast<uint32_t*>(&lo2);
-    packed.y = *reinterpret_cast<uint32_t*>(&hi2);
-    *reinterpret_cast<uint2*>(p.out + row * kHeadDim + 4 * lane) = packed;
-    if (p.lse && lane == 0) p.lse[row] = (mx + __log2f(sum)) * kLn2;
+    const int np = P > 0 ? p.prefix_splits : 0;
+    merge_row(p.ws_lse + row * p.num_splits, p.ws_o + row * p.num_splits * kHeadDim, nsplit,
+              np ? p.prefix_lse + row * np : nullptr,
+              np ? p.prefix_o + row * np * kHeadDim : nullptr, np, p.out + row * kHeadDim,
+              p.lse ? p.lse + row : nullptr, lane);
   }
   if (tid == 0) *counter = 0u;  // ready for the next call
 }
@@ -532,6 +543,20 @@ int plan_decode(int B, int Hq, int Hkv, int max_blocks_per_seq, int num_splits,
   plan->split_blocks = split_blocks;
   plan->num_splits = S;
   plan->prefix_offset = 0;
+  plan->prefix_splits = 0;
+  plan->prefix_kt_per = 0;
+  if (prefix_blocks > 0) {
+    // Key ranges of the shared-prefix pass: enough blocks for about one wave.
+    const int kt = prefix_blocks * (kBlockSize / 128);
+    const int row_pairs = ((B * g + 127) / 128 + 1) / 2;
+    const int base = row_pairs * Hkv;
+    const int sms = sm_count > 0 ? sm_count : 148;
+    int ps = base >= sms ? 1 : sms / base;
+    if (ps > kt) ps = kt;
+    if (ps < 1) ps = 1;
+    plan->prefix_kt_per = (kt + ps - 1) / ps;
+    plan->prefix_splits = (kt + plan->prefix_kt_per - 1) / plan->prefix_kt_per;
+  }
   if (S == 1 && prefix_blocks == 0) {
     plan->workspace_bytes = 0;
   } else {
@@ -542,7 +567,7 @@ int plan_decode(int B, int Hq, int Hkv, int max_blocks_per_seq, int num_splits,
     bytes += align_up(rows * sizeof(float), 256);
     if (prefix_blocks > 0) {
       plan->prefix_offset = bytes;
-      const size_t prow = static_cast<size_t>(B) * Hq;
+      const size_t prow = static_cast<size_t>(B) * Hq * plan->prefix_splits;
       bytes += align_up(prow * kHeadDim * sizeof(float), 256);
       bytes += align_up(prow * sizeof(float), 256);
     }
@@ -576,13 +601,15 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
   prm.num_blocks = a.num_blocks;
   prm.scale_log2 = a.scale * 1.4426950408889634f;
   prm.prefix_tokens = a.prefix_tokens;
+  prm.prefix_splits = plan.prefix_splits;
   prm.prefix_o = nullptr;
   prm.prefix_lse = nullptr;
   if (a.prefix_tokens > 0) {
     const uint8_t* base = static_cast<const uint8_t*>(a.workspace) + plan.prefix_offset;
     prm.prefix_o = reinterpret_cast<const float*>(base);
     prm.prefix_lse = reinterpret_cast<const float*>(
-        base + align_up(static_cast<size_t>(a.B) * a.Hq * kHeadDim * sizeof(float), 256));
+        base + align_up(static_cast<size_t>(a.B) * a.Hq * plan.prefix_splits * kHeadDim *
+                            sizeof(float), 256));
   }
   if (plan.workspace_bytes > 0) {
     const size_t rows = static_cast<size_t>(a.B) * a.Hq * plan.num_splits;

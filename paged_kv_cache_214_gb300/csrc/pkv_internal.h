@@ -42,6 +42,9 @@ struct StoreArgs {
   int64_t num_slots;
 };
 int launch_store(const StoreArgs& a, unsigned* err, cudaStream_t stream);
+int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst,
+                       int n_pairs, int64_t block_bytes, int64_t num_blocks, unsigned* err,
+                       cudaStream_t stream);
 
 struct DecodeArgs {
   void* out;
@@ -68,6 +71,8 @@ struct DecodePlan {
   int split_blocks;   // whole KV blocks per split
   int num_splits;     // S
   size_t prefix_offset;  // byte offset of the shared-prefix partials (if any)
+  int prefix_splits;     // key ranges of the shared-prefix pass
+  int prefix_kt_per;     // 128-key tiles per range
   size_t workspace_bytes;
 };
 // Returns PKV_OK and fills `plan`, or a negative status.  prefix_blocks: blocks
@@ -87,6 +92,8 @@ struct PrefixArgs {
   const int32_t* block_tables;
   int B, Hq, Hkv;
   int prefix_tokens;
+  int splits;   // key ranges; partials are [B*Hq, splits, 128] and [B*Hq, splits]
+  int kt_per;   // 128-key tiles per range
   int64_t num_blocks;
   float scale;
 };

@@ -85,6 +85,7 @@ struct PrefillParams {
   float* part_o;     // shared-prefix mode: [B*Hq, 128] normalised partial
   float* part_lse;   // shared-prefix mode: [B*Hq] log2-sum-exp
   int prefix_tokens; // shared-prefix mode: keys = the first prefix_tokens of table row 0
+  int prefix_kt_per; // shared-prefix mode: key tiles per block (blockIdx.z = key range)
   const __nv_bfloat16* q;
   const int32_t* block_tables;
   const int32_t* cu_q;
@@ -131,18 +132,21 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
   int qt[2], hd[2], rows[2], diag[2], nkt[2];
   int kvh;
   const int32_t* table;
+  int kt0 = 0;   // first key tile of this block (shared-prefix mode splits the keys)
   if constexpr (kPrefix) {
     kvh = blockIdx.y;
     table = p.block_tables;
     const int R = p.B * g;
     Lk = p.prefix_tokens;
+    kt0 = blockIdx.z * p.prefix_kt_per;
+    const int n_here = min(p.prefix_kt_per, p.prefix_tokens / kN - kt0);
 #pragma unroll
     for (int x = 0; x < 2; ++x) {
       qt[x] = 2 * blockIdx.x + x;           // row tile of the group's B*g rows
       hd[x] = 0;
       rows[x] = max(0, min(kM, R - qt[x] * kM));
       diag[x] = INT32_MAX / 2;              // no mask
-      nkt[x] = rows[x] > 0 ? p.prefix_tokens / kN : 0;
+      nkt[x] = rows[x] > 0 ? max(n_here, 0) : 0;
     }
   } else {
     q_begin = p.cu_q[b];
@@ -234,12 +238,13 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
       for (; kt < n_max && !flags[0]; ++kt) {
         const int st = kt & 1;
         const uint32_t ph = ((kt >> 1) - 1) & 1;
-        int id = __ldg(table + (kt >> 1));
+        const int gkt = kt0 + kt;   // key tile within the sequence
+        int id = __ldg(table + (gkt >> 1));
         if (id < 0 || id >= p.num_blocks) {
           record_error(p.err, kErrIndex);
           id = 0;
         }
-        const int slot = id * kBlockSize + (kt & 1) * kN;
+        const int slot = id * kBlockSize + (gkt & 1) * kN;
         if (kt >= 2 && !mbar_wait(bar(kBarKEmpty + st), ph)) break;
         const uint32_t kdst = sbase + kOffK + st * kTile;
         mbar_arrive_expect_tx(bar(kBarKFull + st), kTile);
@@ -450,7 +455,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
           tmem_ld32_wait(o_col + c4 * 32, r);
           if (!valid) continue;
           if constexpr (kPrefix) {
-            float4* dst = reinterpret_cast<float4*>(p.part_o + row * kHeadDim) + c4 * 8;
+            const int64_t prow = row * gridDim.z + blockIdx.z;
+            float4* dst = reinterpret_cast<float4*>(p.part_o + prow * kHeadDim) + c4 * 8;
 #pragma unroll
             for (int k = 0; k < 8; ++k)
               dst[k] = make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
@@ -475,7 +481,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
         }
         if (valid) {
           if constexpr (kPrefix) {
-            p.part_lse[row] = m + __log2f(l);
+            p.part_lse[row * gridDim.z + blockIdx.z] = m + __log2f(l);
           } else {
             if (p.lse) p.lse[row] = (m + __log2f(l)) * kLn2;
           }
@@ -569,6 +575,7 @@ int launch_prefix_attention(const PrefixArgs& a, unsigned* err, cudaStream_t str
   prm.part_o = a.part_o;
   prm.part_lse = a.part_lse;
   prm.prefix_tokens = a.prefix_tokens;
+  prm.prefix_kt_per = a.kt_per;
   prm.q = static_cast<const __nv_bfloat16*>(a.q);
   prm.block_tables = a.block_tables;
   prm.err = err;
@@ -580,7 +587,7 @@ int launch_prefix_attention(const PrefixArgs& a, unsigned* err, cudaStream_t str
   if (!set_smem_attr<true>()) return PKV_ERR_LAUNCH;
   const int rows = a.B * (a.Hq / a.Hkv);
   const int tiles = (rows + kM - 1) / kM;
-  dim3 grid((tiles + 1) / 2, a.Hkv, 1);
+  dim3 grid((tiles + 1) / 2, a.Hkv, a.splits);
   paged_prefill_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(km, vm, prm);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }

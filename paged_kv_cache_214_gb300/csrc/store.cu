@@ -55,7 +55,49 @@ kv_store_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
   }
 }
 
+// Whole-block copies for copy-on-write: block dst[i] of both pools becomes a
+// bit copy of block src[i].  Consecutive threads move consecutive 16-byte pieces.
+__global__ void __launch_bounds__(kStoreThreads)
+kv_copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                      const int32_t* __restrict__ src, const int32_t* __restrict__ dst,
+                      int n_pairs, int64_t block_vecs, int64_t num_blocks, unsigned* err) {
+  const int64_t per_pair = 2 * block_vecs;
+  const int64_t total = static_cast<int64_t>(n_pairs) * per_pair;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const int64_t pair = i / per_pair;
+    const int64_t rem = i - pair * per_pair;
+    const int which = rem >= block_vecs;
+    const int64_t off = rem - which * block_vecs;
+    const int64_t s = __ldg(src + pair), d = __ldg(dst + pair);
+    if (s < 0 || d < 0 || s >= num_blocks || d >= num_blocks) {
+      if (off == 0 && which == 0) record_error(err, kErrIndex);
+      continue;
+    }
+    uint4* cache = which ? v_cache : k_cache;
+    cache[d * block_vecs + off] = cache[s * block_vecs + off];
+  }
+}
+
 }  // namespace
+
+int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst,
+                       int n_pairs, int64_t block_bytes, int64_t num_blocks, unsigned* err,
+                       cudaStream_t stream) {
+  if (n_pairs == 0) return PKV_OK;
+  const int64_t vecs = block_bytes / 16;
+  const int64_t total = static_cast<int64_t>(n_pairs) * 2 * vecs;
+  int sms = device_sm_count();
+  if (sms <= 0) sms = 148;
+  int64_t blocks = (total + kStoreThreads - 1) / kStoreThreads;
+  const int64_t cap = static_cast<int64_t>(sms) * 16;
+  if (blocks > cap) blocks = cap;
+  kv_copy_blocks_kernel<<<static_cast<unsigned>(blocks), kStoreThreads, 0, stream>>>(
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), src, dst, n_pairs, vecs,
+      num_blocks, err);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+}
 
 int launch_store(const StoreArgs& a, unsigned* err, cudaStream_t stream) {
   if (a.T == 0) return PKV_OK;

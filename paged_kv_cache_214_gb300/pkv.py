@@ -53,6 +53,8 @@ def load_library(path: str = LIB_PATH):
                                 ctypes.c_float, ctypes.c_size_t)
         lib.kv_cache_store.argtypes = [P, P, i64, i64, P, P, P, i64, i32, i32, i32, i64, P]
         lib.kv_cache_store.restype = i32
+        lib.kv_cache_copy_blocks.argtypes = [P, P, P, P, i32, i32, i32, i32, i64, P]
+        lib.kv_cache_copy_blocks.restype = i32
         lib.paged_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
         lib.paged_decode_workspace_bytes.restype = sz
         lib.paged_decode_num_splits.argtypes = [i32, i32, i32, i32, i32, i32, i32]
@@ -141,6 +143,22 @@ def kv_cache_store(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
     _check(lib.kv_cache_store(_ptr(k), _ptr(v), k.stride(0), v.stride(0), _ptr(k_cache),
                               _ptr(v_cache), _ptr(slot_mapping), T, Hkv, D, bs, NB,
                               _stream(stream)), "kv_cache_store")
+
+
+def kv_cache_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor,
+                         src_blocks: torch.Tensor, dst_blocks: torch.Tensor,
+                         stream=None) -> None:
+    """Copy-on-write copies: block dst_blocks[i] of both caches becomes a copy
+    of block src_blocks[i] (int32 device tensors of equal length)."""
+    lib = load_library()
+    NB, bs, Hkv, D = _pool_dims(k_cache, v_cache)
+    _need(src_blocks, "src_blocks", torch.int32, 1)
+    _need(dst_blocks, "dst_blocks", torch.int32, 1)
+    if src_blocks.shape != dst_blocks.shape:
+        raise ValueError("src_blocks and dst_blocks differ in length")
+    _check(lib.kv_cache_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(src_blocks),
+                                    _ptr(dst_blocks), src_blocks.shape[0], Hkv, D, bs, NB,
+                                    _stream(stream)), "kv_cache_copy_blocks")
 
 
 def paged_decode_workspace_bytes(B: int, Hq: int, Hkv: int, D: int, max_blocks_per_seq: int,

@@ -128,6 +128,29 @@ def pin_store_roundtrip(lib):
     assert np.array_equal(K, kk) and np.array_equal(V, vv)
 
 
+def pin_copy_blocks(lib):
+    """Copy-on-write copies: the destination block reads back as the source
+    (through a table that points at it), nothing else changes, and an
+    out-of-range id is rejected without a change."""
+    gen = torch.Generator().manual_seed(16)
+    NB, bs, Hkv = 6, 16, 2
+    kc = _bits(_bf16((NB, bs, Hkv, D), gen)).copy()
+    vc = _bits(_bf16((NB, bs, Hkv, D), gen)).copy()
+    k0, v0 = kc.copy(), vc.copy()
+    O.copy_blocks(kc, vc, [2, 4], [5, 0], lib=lib)
+    K_src, V_src = O.gather(k0, v0, np.array([2, 4], np.int32), 2 * bs, lib=lib)
+    K_dst, V_dst = O.gather(kc, vc, np.array([5, 0], np.int32), 2 * bs, lib=lib)
+    assert np.array_equal(K_src, K_dst) and np.array_equal(V_src, V_dst)
+    for b in (1, 2, 3, 4):
+        assert np.array_equal(kc[b], k0[b]) and np.array_equal(vc[b], v0[b])
+    try:
+        O.copy_blocks(kc, vc, [1], [NB], lib=lib)
+    except O.OracleError:
+        pass
+    else:
+        raise AssertionError("an out-of-range block id was accepted")
+
+
 def pin_store_rejects(lib):
     gen = torch.Generator().manual_seed(2)
     NB, bs, Hkv = 2, 256, 1
@@ -409,6 +432,7 @@ def pin_prefill_rejects_lk_lt_lq(lib):
 ALL_PINS = [
     pin_store_roundtrip,
     pin_store_rejects,
+    pin_copy_blocks,
     pin_decode_bruteforce,
     pin_decode_sdpa,
     pin_decode_closed_forms,

@@ -77,3 +77,20 @@ def test_status_strings(lib):
     for code in range(-6, 1):
         assert pkv.status_string(code).startswith("PKV_")
     assert "unknown" in pkv.status_string(42)
+
+
+def test_bindings_declare_every_signature(lib):
+    """ctypes passes undeclared integer arguments as 32-bit ints, which would
+    truncate 64-bit device pointers: every exported function must carry
+    argtypes / restype from the bindings."""
+    from paged_kv_cache_214_gb300 import blocks
+    blocks._lib()
+    hdr_dir = os.path.dirname(HEADER)
+    for header in ("pkv.h", "pkv_blocks.h"):
+        text = re.sub(r"/\*.*?\*/", "", open(os.path.join(hdr_dir, header)).read(), flags=re.S)
+        names = re.findall(r"^\s*(?:int|int64_t|size_t|void|const char\s*\*|pkv_block_manager\s*\*)"
+                           r"\s*(\w+)\s*\(", text, flags=re.M)
+        assert names, header
+        for name in names:
+            fn = getattr(lib, name)
+            assert fn.argtypes is not None, f"{name} has no argtypes"

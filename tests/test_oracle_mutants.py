@@ -38,6 +38,12 @@ MUTANTS = [
     ("store-k-into-v", "std::memcpy(v_cache + dst, v + t * v_tok_stride, sizeof(uint16_t) * row);",
      "std::memcpy(v_cache + dst, k + t * k_tok_stride, sizeof(uint16_t) * row);"),
     ("store-no-duplicate-check", "if (seen[s]) return -3;", "if (false) return -3;"),
+    ("copy-blocks-k-from-v",
+     "std::memcpy(k_cache + dst[i] * block_elems, k_cache + src[i] * block_elems,",
+     "std::memcpy(k_cache + dst[i] * block_elems, v_cache + src[i] * block_elems,"),
+    ("copy-blocks-wrong-direction",
+     "std::memcpy(v_cache + dst[i] * block_elems, v_cache + src[i] * block_elems,",
+     "std::memcpy(v_cache + src[i] * block_elems, v_cache + dst[i] * block_elems,"),
     ("prefill-wrong-q-row", "const int64_t o = row * Hq + h;",
      "const int64_t o = row * Hq + hh;"),
     ("softmax-max-not-subtracted-from-weights", "s[j] = std::exp(s[j] - m);",
