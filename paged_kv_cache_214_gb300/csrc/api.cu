@@ -59,7 +59,7 @@ unsigned* device_error_word() {
 }
 
 bool encode_pool_map(CUtensorMap* map, const void* base, int64_t num_slots, int Hkv,
-                     int box_rows) {
+                     int box_rows, int box_heads) {
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_encode) {
@@ -73,12 +73,13 @@ bool encode_pool_map(CUtensorMap* map, const void* base, int64_t num_slots, int 
     }
   }
   // [slots, Hkv, D] with D innermost; a box is 64 dims (128 B, the swizzle
-  // span) x 1 head x box_rows consecutive slots.
+  // span) x box_heads heads x box_rows consecutive slots.
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(Hkv),
                               static_cast<cuuint64_t>(num_slots)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
                                  static_cast<cuuint64_t>(Hkv) * kHeadDim * 2};
-  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_heads),
+                             static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
                               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

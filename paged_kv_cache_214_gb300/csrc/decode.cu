@@ -138,7 +138,7 @@ __device__ __forceinline__ float rescale(float m, float mn) {
   return m == -INFINITY ? 0.f : ex2(m - mn);
 }
 
-template <int G>
+template <int G, int KVH>
 __global__ void __launch_bounds__(kThreads, 2)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
@@ -155,11 +155,18 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
 
+  // KVH kv heads per block: each pipeline stage holds kTT tokens x KVH heads
+  // (so a token contributes one contiguous KVH x 256-byte chunk), and
+  // kWPH = 4 / KVH warps work on each of the block's kv heads.
+  constexpr int kTT = kTile / KVH;
+  constexpr int kWPH = kConsumerWarps / KVH;
   const int split = blockIdx.x;
-  const int hg = blockIdx.y;  // kv head * head_groups + head group
+  const int hg = blockIdx.y;  // (kv head group of KVH) * head_groups + query head group
   const int b = blockIdx.z;
-  const int kvh = hg / p.head_groups;
-  const int h0 = kvh * (p.Hq / p.Hkv) + (hg % p.head_groups) * G;  // first query head
+  const int g = p.Hq / p.Hkv;
+  const int kvh0 = (hg / p.head_groups) * KVH;   // first kv head of the block
+  const int hoff = (hg % p.head_groups) * G;     // first query head within each group
+  auto qhead = [&](int hh, int h) { return (kvh0 + hh) * g + hoff + h; };
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -192,40 +199,42 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 
   if (ctx == P) {  // nothing past the prefix: out = the prefix's result (or 0, -inf)
     if (P > 0) {
-      for (int h = warp; h < G; h += kConsumerWarps) {
-        const int64_t row = static_cast<int64_t>(b) * p.Hq + h0 + h;
+      for (int r = warp; r < KVH * G; r += kConsumerWarps) {
+        const int64_t row = static_cast<int64_t>(b) * p.Hq + qhead(r / G, r % G);
         const int np = p.prefix_splits;
         merge_row(nullptr, nullptr, 0, p.prefix_lse + row * np, p.prefix_o + row * np * kHeadDim,
                   np, p.out + row * kHeadDim, p.lse ? p.lse + row : nullptr, lane);
       }
       return;
     }
-    for (int i = tid; i < G * kHeadDim; i += kThreads) {
-      const int h = i / kHeadDim, d = i % kHeadDim;
-      p.out[(static_cast<int64_t>(b) * p.Hq + h0 + h) * kHeadDim + d] = __float2bfloat16_rn(0.f);
+    for (int i = tid; i < KVH * G * kHeadDim; i += kThreads) {
+      const int r = i / kHeadDim, d = i % kHeadDim;
+      p.out[(static_cast<int64_t>(b) * p.Hq + qhead(r / G, r % G)) * kHeadDim + d] =
+          __float2bfloat16_rn(0.f);
     }
-    if (p.lse && tid < G) p.lse[static_cast<int64_t>(b) * p.Hq + h0 + tid] = -INFINITY;
+    if (p.lse && tid < KVH * G)
+      p.lse[static_cast<int64_t>(b) * p.Hq + qhead(tid / G, tid % G)] = -INFINITY;
     return;
   }
 
   const int tok_begin = P + split * split_tokens;
   const int tok_end = min(ctx, tok_begin + split_tokens);
-  const int n_tiles = (tok_end - tok_begin + kTile - 1) / kTile;
+  const int n_tiles = (tok_end - tok_begin + kTT - 1) / kTT;
 
   // Lane 0 of warp 0 is the producer: it fills the ring up front and refills a
   // stage as soon as all four warps have released it.
   const uint64_t policy = l2_policy_evict_first();
   auto issue = [&](int it) {
     const int s = it % kStages;
-    const int tok = tok_begin + it * kTile;
+    const int tok = tok_begin + it * kTT;
     const int slot = sblk[tok / kBlockSize - blk_begin] * kBlockSize + tok % kBlockSize;
     const uint32_t kdst = smem_addr(smem + s * kStageBytes);
     const uint32_t vdst = kdst + kOperandBytes;
     mbar_arrive_expect_tx(full_bar(s), kStageBytes);
-    tma_load_3d_hint(kdst, &kmap, full_bar(s), 0, kvh, slot, policy);
-    tma_load_3d_hint(kdst + kHalfBytes, &kmap, full_bar(s), 64, kvh, slot, policy);
-    tma_load_3d_hint(vdst, &vmap, full_bar(s), 0, kvh, slot, policy);
-    tma_load_3d_hint(vdst + kHalfBytes, &vmap, full_bar(s), 64, kvh, slot, policy);
+    tma_load_3d_hint(kdst, &kmap, full_bar(s), 0, kvh0, slot, policy);
+    tma_load_3d_hint(kdst + kHalfBytes, &kmap, full_bar(s), 64, kvh0, slot, policy);
+    tma_load_3d_hint(vdst, &vmap, full_bar(s), 0, kvh0, slot, policy);
+    tma_load_3d_hint(vdst + kHalfBytes, &vmap, full_bar(s), 64, kvh0, slot, policy);
     flags[2] = it + 1;
   };
   if (warp == 0) {
@@ -260,12 +269,17 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     // ------------------------------------------------------------ consumers
     const int grp = lane >> 3;  // group within the warp
     const int j = lane & 7;     // lane within the group: dims [8j,8j+8) and [64+8j,64+8j+8)
+    const int my_hh = warp / kWPH;   // this warp's kv head within the block
+    const int my_wl = warp % kWPH;   // this warp's index among that head's warps
+    // Tile row r (0..3) of this group is token 4*(r*kWPH + my_wl) + grp of the
+    // stage, held in shared-memory row token*KVH + my_hh (128-byte rows).
     // q (pre-scaled into base-2 units) and the running output, as fp32 pairs:
     // pair i < 4 covers dims 8j+2i, 8j+2i+1; pair i >= 4 covers 64+8j+2(i-4), +1.
     f32x2 q2[G][8];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const __nv_bfloat16* qp = p.q + (static_cast<int64_t>(b) * p.Hq + h0 + h) * kHeadDim;
+      const __nv_bfloat16* qp =
+          p.q + (static_cast<int64_t>(b) * p.Hq + qhead(my_hh, h)) * kHeadDim;
       const uint4 a = __ldg(reinterpret_cast<const uint4*>(qp + 8 * j));
       const uint4 c = __ldg(reinterpret_cast<const uint4*>(qp + 64 + 8 * j));
       const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
@@ -291,7 +305,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         flags[0] = 1;
         break;
       }
-      const int n_valid = min(kTile, tok_end - (tok_begin + it * kTile));
+      const int n_valid = min(kTT, tok_end - (tok_begin + it * kTT));
       const uint32_t kb = smem_addr(smem + s * kStageBytes);
       const uint32_t vb = kb + kOperandBytes;
 
@@ -299,8 +313,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       float sc[4][G];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int t = 16 * r + 4 * warp + grp;
-        const uint32_t off = t * 128 + ((j ^ (t & 7)) << 4);
+        const int t = 4 * (r * kWPH + my_wl) + grp;
+        const int srow = t * KVH + my_hh;
+        const uint32_t off = srow * 128 + ((j ^ (srow & 7)) << 4);
         const uint4 k0 = lds128(kb + off);
         const uint4 k1 = lds128(kb + kHalfBytes + off);
         const uint32_t w[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
@@ -340,16 +355,17 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         }
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          const int t = 16 * r + 4 * warp + grp;
+          const int t = 4 * (r * kWPH + my_wl) + grp;
           sc[r][h] = t < n_valid ? ex2(sc[r][h] - m[h]) : 0.f;
           l[h] += sc[r][h];
         }
       }
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int t = 16 * r + 4 * warp + grp;
+        const int t = 4 * (r * kWPH + my_wl) + grp;
         if (t < n_valid) {
-          const uint32_t off = t * 128 + ((j ^ (t & 7)) << 4);
+          const int srow = t * KVH + my_hh;
+          const uint32_t off = srow * 128 + ((j ^ (srow & 7)) << 4);
           const uint4 v0 = lds128(vb + off);
           const uint4 v1 = lds128(vb + kHalfBytes + off);
           const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -438,20 +454,21 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   // thread tid (0..127) owns dim d = tid of every head
   const int d = tid;
   const bool single = nsplit == 1 && P == 0;
-  for (int h = 0; h < G; ++h) {
+  for (int r = 0; r < KVH * G; ++r) {
+    const int hh = r / G, h = r % G;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge_m[w * G + h]);
+    for (int w = hh * kWPH; w < (hh + 1) * kWPH; ++w) M = fmaxf(M, merge_m[w * G + h]);
     float Ls = 0.f, Os = 0.f;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
+    for (int w = hh * kWPH; w < (hh + 1) * kWPH; ++w) {
       const float c = rescale(merge_m[w * G + h], M);
       Ls += merge_l[w * G + h] * c;
       Os += merge_o[(w * G + h) * kHeadDim + d] * c;
     }
     const float on = Os / Ls;
     const float lse2 = M + __log2f(Ls);
-    const int64_t row = static_cast<int64_t>(b) * p.Hq + h0 + h;
+    const int64_t row = static_cast<int64_t>(b) * p.Hq + qhead(hh, h);
     if (single) {
       p.out[row * kHeadDim + d] = __float2bfloat16_rn(on);
       if (p.lse && d == 0) p.lse[row] = lse2 * kLn2;
@@ -467,7 +484,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   // All partial stores of the block precede the barrier; one thread then
   // publishes them at device scope and takes the ticket.
   named_barrier(1, kConsumerWarps * 32);
-  unsigned* counter = p.ws_count + static_cast<int64_t>(b) * p.Hkv * p.head_groups + hg;
+  unsigned* counter = p.ws_count + static_cast<int64_t>(b) * gridDim.y + hg;
   if (tid == 0) {
     __threadfence();
     const unsigned ticket = atomicAdd(counter, 1u);
@@ -477,8 +494,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   }
   named_barrier(1, kConsumerWarps * 32);
   if (!flags[1]) return;
-  for (int h = warp; h < G; h += kConsumerWarps) {
-    const int64_t row = static_cast<int64_t>(b) * p.Hq + h0 + h;
+  for (int r = warp; r < KVH * G; r += kConsumerWarps) {
+    const int64_t row = static_cast<int64_t>(b) * p.Hq + qhead(r / G, r % G);
     const int np = P > 0 ? p.prefix_splits : 0;
     merge_row(p.ws_lse + row * p.num_splits, p.ws_o + row * p.num_splits * kHeadDim, nsplit,
               np ? p.prefix_lse + row * np : nullptr,
@@ -488,7 +505,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   if (tid == 0) *counter = 0u;  // ready for the next call
 }
 
-template <int G>
+template <int G, int KVH>
 int launch_g(const DecodeArgs& a, const DecodePlan& plan, const DecodeParams& prm,
              const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t stream) {
   using L = SmemLayout<G>;
@@ -497,13 +514,13 @@ int launch_g(const DecodeArgs& a, const DecodePlan& plan, const DecodeParams& pr
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(paged_decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(paged_decode_kernel<G, KVH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::kBytes) != cudaSuccess)
       return PKV_ERR_LAUNCH;
     attr_set[dev] = true;
   }
-  dim3 grid(plan.num_splits, a.Hkv * plan.head_groups, a.B);
-  paged_decode_kernel<G><<<grid, kThreads, L::kBytes, stream>>>(km, vm, prm);
+  dim3 grid(plan.num_splits, (a.Hkv / KVH) * plan.head_groups, a.B);
+  paged_decode_kernel<G, KVH><<<grid, kThreads, L::kBytes, stream>>>(km, vm, prm);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }
 
@@ -521,6 +538,11 @@ int plan_decode(int B, int Hq, int Hkv, int max_blocks_per_seq, int num_splits,
   const int G = (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1;
   plan->heads_per_cta = G;
   plan->head_groups = g / G;
+  // One kv head per block.  (The kernel also reads KVH = 2 heads per block as
+  // 512-byte chunks per token; on GB300 that measured 2% slower on the
+  // batch-64 decode and slower on short contexts, so it is not selected.)
+  plan->kv_per_cta = 1;
+  const int kv_groups = Hkv / plan->kv_per_cta;
   const int rest = max_blocks_per_seq - prefix_blocks;
   const int maxblk = rest > 0 ? rest : 1;
   int split_blocks;
@@ -529,7 +551,7 @@ int plan_decode(int B, int Hq, int Hkv, int max_blocks_per_seq, int num_splits,
   } else {
     // Enough (sequence, head group, split) units for about eight waves of two
     // blocks per SM if every context were full length; whole blocks per split.
-    const int64_t units = static_cast<int64_t>(B) * Hkv * plan->head_groups * maxblk;
+    const int64_t units = static_cast<int64_t>(B) * kv_groups * plan->head_groups * maxblk;
     const int64_t target = static_cast<int64_t>(sm_count > 0 ? sm_count : 148) * 2 * 8;
     split_blocks = static_cast<int>((units + target - 1) / target);
     if (split_blocks < 2) split_blocks = maxblk < 2 ? maxblk : 2;
@@ -560,7 +582,8 @@ int plan_decode(int B, int Hq, int Hkv, int max_blocks_per_seq, int num_splits,
   if (S == 1 && prefix_blocks == 0) {
     plan->workspace_bytes = 0;
   } else {
-    if (static_cast<int64_t>(B) * Hkv * plan->head_groups > kMaxCounters) return PKV_ERR_SHAPE;
+    if (static_cast<int64_t>(B) * kv_groups * plan->head_groups > kMaxCounters)
+      return PKV_ERR_SHAPE;
     const size_t rows = static_cast<size_t>(B) * Hq * S;
     size_t bytes = kCounterRegion;
     bytes += align_up(rows * kHeadDim * sizeof(float), 256);
@@ -581,8 +604,9 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
   if (a.B == 0) return PKV_OK;
   CUtensorMap km, vm;
   const int64_t slots = a.num_blocks * kBlockSize;
-  if (!encode_pool_map(&km, a.k_cache, slots, a.Hkv, kTile) ||
-      !encode_pool_map(&vm, a.v_cache, slots, a.Hkv, kTile))
+  const int kvh = plan.kv_per_cta;
+  if (!encode_pool_map(&km, a.k_cache, slots, a.Hkv, kTile / kvh, kvh) ||
+      !encode_pool_map(&vm, a.v_cache, slots, a.Hkv, kTile / kvh, kvh))
     return PKV_ERR_ARG;
   DecodeParams prm;
   prm.out = static_cast<__nv_bfloat16*>(a.out);
@@ -625,9 +649,9 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
     prm.ws_count = nullptr;
   }
   switch (plan.heads_per_cta) {
-    case 4: return launch_g<4>(a, plan, prm, km, vm, stream);
-    case 2: return launch_g<2>(a, plan, prm, km, vm, stream);
-    default: return launch_g<1>(a, plan, prm, km, vm, stream);
+    case 4: return launch_g<4, 1>(a, plan, prm, km, vm, stream);
+    case 2: return launch_g<2, 1>(a, plan, prm, km, vm, stream);
+    default: return launch_g<1, 1>(a, plan, prm, km, vm, stream);
   }
 }
 

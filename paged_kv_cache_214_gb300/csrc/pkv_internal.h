@@ -25,9 +25,9 @@ int device_sm_count();
 unsigned* device_error_word();
 
 // Tensor map over one pool tensor viewed as [slots, Hkv, D] (D innermost),
-// box = {64 elements of D, 1 head, box_rows slots}, 128-byte swizzle.
+// box = {64 elements of D, box_heads heads, box_rows slots}, 128-byte swizzle.
 bool encode_pool_map(CUtensorMap* map, const void* base, int64_t num_slots, int Hkv,
-                     int box_rows);
+                     int box_rows, int box_heads = 1);
 
 struct StoreArgs {
   const void* k;
@@ -66,7 +66,8 @@ struct DecodeArgs {
 
 // Split plan of one decode call.
 struct DecodePlan {
-  int heads_per_cta;  // G: query heads that one thread block serves
+  int kv_per_cta;     // KVH: kv heads one thread block reads (1, 2 or 4)
+  int heads_per_cta;  // G: query heads per kv head that one thread block serves
   int head_groups;    // (Hq/Hkv) / G
   int split_blocks;   // whole KV blocks per split
   int num_splits;     // S
