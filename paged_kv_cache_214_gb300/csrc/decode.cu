@@ -47,6 +47,7 @@ constexpr int kTile = 64;                       // tokens per pipeline stage
 constexpr int kStages = 3;
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = kConsumerWarps * 32;
+static_assert(kConsumerWarps == 4, "each warp loads one quarter (K or V, one 64-dim half) of a stage");
 constexpr int kHalfBytes = kTile * 128;         // 64 rows x 64 dims x 2 B
 constexpr int kOperandBytes = 2 * kHalfBytes;   // one of K or V for a tile
 constexpr int kStageBytes = 2 * kOperandBytes;  // K and V
@@ -221,26 +222,29 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   const int tok_end = min(ctx, tok_begin + split_tokens);
   const int n_tiles = (tok_end - tok_begin + kTT - 1) / kTT;
 
-  // Lane 0 of warp 0 is the producer: it fills the ring up front and refills a
-  // stage as soon as all four warps have released it.
+  // Every warp is a producer for one quarter of each stage (warp w loads
+  // K dims [0,64), K [64,128), V [0,64), V [64,128) for w = 0..3): one thread
+  // streams its tensor copies one after another at a few hundred cycles each,
+  // so four issuing threads land a stage sooner than one.  Lane 0 of each warp
+  // fills its quarter of the ring up front and refills it as soon as all four
+  // warps have released the stage.
   const uint64_t policy = l2_policy_evict_first();
   auto issue = [&](int it) {
     const int s = it % kStages;
     const int tok = tok_begin + it * kTT;
     const int slot = sblk[tok / kBlockSize - blk_begin] * kBlockSize + tok % kBlockSize;
-    const uint32_t kdst = smem_addr(smem + s * kStageBytes);
-    const uint32_t vdst = kdst + kOperandBytes;
-    mbar_arrive_expect_tx(full_bar(s), kStageBytes);
-    tma_load_3d_hint(kdst, &kmap, full_bar(s), 0, kvh0, slot, policy);
-    tma_load_3d_hint(kdst + kHalfBytes, &kmap, full_bar(s), 64, kvh0, slot, policy);
-    tma_load_3d_hint(vdst, &vmap, full_bar(s), 0, kvh0, slot, policy);
-    tma_load_3d_hint(vdst + kHalfBytes, &vmap, full_bar(s), 64, kvh0, slot, policy);
-    flags[2] = it + 1;
+    const uint32_t dst = smem_addr(smem + s * kStageBytes) + warp * kHalfBytes;
+    mbar_arrive_expect_tx(full_bar(s), kHalfBytes);
+    if (warp < 2)
+      tma_load_3d_hint(dst, &kmap, full_bar(s), (warp & 1) * 64, kvh0, slot, policy);
+    else
+      tma_load_3d_hint(dst, &vmap, full_bar(s), (warp & 1) * 64, kvh0, slot, policy);
+    atomicMax(const_cast<int*>(flags + 2), it + 1);
   };
   if (warp == 0) {
     if (lane == 0) {
       for (int s = 0; s < kStages; ++s) {
-        mbar_init(full_bar(s), 1);
+        mbar_init(full_bar(s), kConsumerWarps);   // one arrival per quarter
         mbar_init(empty_bar(s), kConsumerWarps);
       }
       flags[0] = 0;  // abort
@@ -258,12 +262,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       }
       sblk[lane] = spec_id;
     }
-    __syncwarp();
-    if (lane == 0) {
-      for (int it = 0; it < kStages && it < n_tiles; ++it) issue(it);
-    }
   }
   __syncthreads();
+  if (lane == 0)
+    for (int it = 0; it < kStages && it < n_tiles; ++it) issue(it);
 
   {
     // ------------------------------------------------------------ consumers
@@ -383,7 +385,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(empty_bar(s));
-        if (warp == 0 && it + kStages < n_tiles && !flags[0]) {
+        if (it + kStages < n_tiles && !flags[0]) {
           if (mbar_wait(empty_bar(s), (it / kStages) & 1)) {
             issue(it + kStages);
           } else {
@@ -570,8 +572,9 @@ int plan_decode(int B, int Hq, int Hkv, int max_blocks_per_seq, int num_splits,
   if (prefix_blocks > 0) {
     // Key ranges of the shared-prefix pass: enough blocks for about one wave.
     const int kt = prefix_blocks * (kBlockSize / 128);
-    const int row_pairs = ((B * g + 127) / 128 + 1) / 2;
-    const int base = row_pairs * Hkv;
+    const int rpt = prefix_rows_per_tile(g);
+    if (rpt == 0) return PKV_ERR_SHAPE;
+    const int base = (B * g + rpt - 1) / rpt * Hkv;   // query tiles of the pass
     const int sms = sm_count > 0 ? sm_count : 148;
     int ps = base >= sms ? 1 : sms / base;
     if (ps > kt) ps = kt;

@@ -99,6 +99,9 @@ struct PrefixArgs {
   float scale;
 };
 int launch_prefix_attention(const PrefixArgs& a, unsigned* err, cudaStream_t stream);
+// (sequence, head) rows per query tile of the shared-prefix pass for a group of
+// g query heads per kv head (whole tokens per tile), or 0 if g is unsupported.
+int prefix_rows_per_tile(int g);
 int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
                   cudaStream_t stream);
 
