@@ -16,23 +16,30 @@
 // first, so that set-up, the first loads and the output stores of one item
 // overlap the next.  Twelve warps, each with one job:
 //   warp 8  (TMA)  Q tiles and 128-key K tiles (two 64-dim boxes, 128-byte
-//                  swizzle); a K tile never straddles a 256-token block.
+//                  swizzle); a K tile never straddles a 256-token block.  The
+//                  next item's Q loads right after its first K tile.
 //   warp 9  (TMA)  V tiles.
 //   warp 10 (MMA)  S_t = Q K_t^T into one of three S buffers in tensor memory.
 //   warp 11 (MMA)  O += P_t V_t, A = P_t read from tensor memory, B = V_t
 //                  MN-major straight from its TMA tile.
-//   warps 0-7      softmax: warp w owns rows 32(w%4).. (its TMEM lane quarter)
-//                  and key columns 64(w/4).. of every S tile.  The two warps of
-//                  a row quarter exchange their partial row maxima through
-//                  shared memory, keep the running max in base 2, rescale O
-//                  only when the max grew by more than 2^8 (weights below 256
-//                  are exact enough in fp32 / bf16), and write P as bf16 pairs
-//                  over the first 64 columns of the tile's S buffer.
+//   warps 0-7      softmax: warp w owns 16 whole rows of every S tile (half of
+//                  its TMEM lane quarter, read with the 16-lane access shapes),
+//                  keeps the running max in base 2, rescales O only when the
+//                  max grew by more than 2^8 (weights below 256 are exact
+//                  enough in fp32 / bf16), and writes P as bf16 pairs over the
+//                  first 64 columns of the tile's S buffer.  No softmax warp
+//                  waits for another, so the exp2 work of one overlaps the
+//                  loads and reductions of the other on the same SM quarter.
 // The MMAs come from two threads: one thread issuing M=N=128 tcgen05.mma in a
 // chain waits ~116 cycles per instruction, about half the tensor pipe, while
 // two independent chains fill it.  S is triple-buffered, so the S of tile t+1
 // (and t+2) is computed while the softmax of tile t runs.
 // TMEM (512 columns): S_0 | S_1 | S_2 | O.
+// K and V each have three 32 KB stages (Q one buffer).  The tensor copies of
+// one thread complete one after another, so every tile copy is split in its
+// two 64-dim boxes issued by two lanes, and each ring stage has lanes of its
+// own: a copy never waits behind the previous tile's.  An item's output is
+// written while the next item's first tile is in flight.
 // Every wait is bounded: a wait that runs out records an error, the block
 // drains what it started, frees its tensor memory and exits.
 
@@ -55,32 +62,32 @@ constexpr int kPVWarp = 11;
 constexpr int kThreads = 12 * 32;
 constexpr int kHalf = 128 * 128;           // 128 rows x 64 bf16 (one 128-byte swizzled box)
 constexpr int kTile = 2 * kHalf;           // 128 rows x 128 bf16
-constexpr int kOffQ = 0;                   // 2 buffers
-constexpr int kOffK = kOffQ + 2 * kTile;   // 2 stages
-constexpr int kOffV = kOffK + 2 * kTile;   // 2 stages
-constexpr int kOffXMax = kOffV + 2 * kTile;          // f32 [2 parity][2 halves][128 rows]
-constexpr int kOffXSum = kOffXMax + 2 * 2 * 128 * 4; // f32 [2 halves][128 rows]
-constexpr int kOffBars = kOffXSum + 2 * 128 * 4;
+constexpr int kKStages = 3;
+constexpr int kVStages = 3;
+constexpr int kOffQ = 0;                              // one buffer
+constexpr int kOffK = kOffQ + kTile;                  // kKStages stages
+constexpr int kOffV = kOffK + kKStages * kTile;       // kVStages stages
+constexpr int kOffBars = kOffV + kVStages * kTile;
 constexpr int kSBufs = 3;
 // barriers
-constexpr int kBarQFull = 0;    // [Q buffer]
-constexpr int kBarQEmpty = 2;   // [Q buffer]
-constexpr int kBarKFull = 4;    // [stage]
-constexpr int kBarKEmpty = 6;   // [stage]
-constexpr int kBarVFull = 8;    // [stage]
-constexpr int kBarVEmpty = 10;  // [stage]
-constexpr int kBarSFull = 12;   // [S buffer] x3
-constexpr int kBarPFull = 15;   // [S buffer] x3, 8 softmax warps
-constexpr int kBarPVDone = 18;  // [S buffer] x3: the PV that read P from it has completed
-constexpr int kBarOFull = 21;   // the last PV of an item has completed
-constexpr int kBarXMax = 22;    // [row quarter][parity]: 2 warps
-constexpr int kBarXSum = 30;    // [row quarter]: 2 warps
-constexpr int kBarDrainS = 34;
-constexpr int kBarDrainPV = 35;
-constexpr int kNumBars = 36;
+constexpr int kBarQFull = 0;
+constexpr int kBarQEmpty = 1;
+constexpr int kBarKFull = 2;    // [K stage]
+constexpr int kBarKEmpty = 5;   // [K stage]
+constexpr int kBarVFull = 8;    // [V stage]
+constexpr int kBarVEmpty = 11;  // [V stage]
+constexpr int kBarSFull = 14;   // [S buffer]
+constexpr int kBarPFull = 17;   // [S buffer], 8 softmax warps
+constexpr int kBarPVDone = 20;  // [S buffer]: the PV that read P from it has completed
+constexpr int kBarOFull = 23;   // the last PV of an item has completed
+constexpr int kBarDrainS = 24;
+constexpr int kBarDrainPV = 25;
+constexpr int kNumBars = 26;
+static_assert(kKStages == 3 && kVStages == 3 && kSBufs == 3, "barrier layout");
 constexpr int kOffTmem = kOffBars + kNumBars * 8;
 constexpr int kOffFlags = kOffTmem + 8;
 constexpr int kSmemBytes = kOffFlags + 16 + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "one block per SM must fit in shared memory");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;      // + 128 * buffer
 constexpr uint32_t kColO = 384;
@@ -182,18 +189,32 @@ __device__ __forceinline__ int item_index(int k) {
   return k * static_cast<int>(gridDim.x) + c;
 }
 
+// First non-empty item at or after round k (k is advanced to it).
+template <bool kPrefix>
+__device__ __forceinline__ bool next_item(const PrefillParams& p, int n_rounds, int& k, Item& it,
+                                          bool report) {
+  for (; k < n_rounds; ++k) {
+    const int idx = item_index(k);
+    if (idx >= p.n_items) continue;
+    it = get_item<kPrefix>(p, idx, report);
+    if (it.n > 0) return true;
+  }
+  return false;
+}
+
 // Wait with every lane of the warp; the result is the same for all lanes.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return __all_sync(kFull, mbar_wait(bar, parity));
 }
 
-// Running position in the three-way S ring: buffer and phase parity.
-struct Ring3 {
-  int buf = 0;
+// Running position in an N-slot ring: slot and phase parity.
+template <int N>
+struct Ring {
+  int idx = 0;
   uint32_t ph = 0;
   __device__ __forceinline__ void next() {
-    if (++buf == kSBufs) {
-      buf = 0;
+    if (++idx == N) {
+      idx = 0;
       ph ^= 1u;
     }
   }
@@ -240,8 +261,6 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
   auto bar = [&](int i) { return bars + 8u * i; };
   volatile int* flags = reinterpret_cast<volatile int*>(smem + kOffFlags);
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + kOffTmem);
-  float* xmax = reinterpret_cast<float*>(smem + kOffXMax);
-  float* xsum = reinterpret_cast<float*>(smem + kOffXSum);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -254,7 +273,6 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t count = 1;
       if (i >= kBarPFull && i < kBarPFull + kSBufs) count = kSoftmaxWarps;
-      if (i >= kBarXMax && i < kBarDrainS) count = 2;   // the two warps of a row quarter
       mbar_init(bar(i), count);
     }
     flags[0] = 0;  // abort
@@ -279,15 +297,15 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
 
   if (warp == kQKWarp) {
     // ------------------------------------------------------------ TMA: Q and K
-    // The Q of an item is loaded while the previous item streams its keys:
-    // right after that item's second K tile (or at the very start).
+    // An item's Q goes into the single Q buffer right after its first K tile
+    // has been issued, once the S MMAs of the previous item are done with it.
     bool ok = true;
     int gi = 0, gk = 0;
     BlockIds ids;
+    Ring<kKStages> rk;
     auto load_q = [&](const Item& it, int qi) -> bool {
-      const int qb = qi & 1;
-      const uint32_t qdst = sbase + kOffQ + qb * kTile;
-      if (qi >= 2 && !warp_wait(bar(kBarQEmpty + qb), ((qi - 2) >> 1) & 1)) return false;
+      const uint32_t qdst = sbase + kOffQ;
+      if (qi >= 1 && !warp_wait(bar(kBarQEmpty), (qi - 1) & 1)) return false;
       if (!kPrefix && it.rows < kM) {
         // ragged last tile of a sequence: gather its rows (zero-fill the rest)
         const __nv_bfloat16* base =
@@ -303,68 +321,56 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
         cp_async_wait_all();
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarQFull + qb));
-      } else if (lane == 0) {
-        if constexpr (kPrefix) {
-          // (sequence, head) rows of the group: box {64 dims, g heads, tokens}
-          mbar_arrive_expect_tx(bar(kBarQFull + qb), p.rows_per_tile * 256);
-          const int tok0 = it.q0 / g;
-          tma_load_3d(qdst, &qmap, bar(kBarQFull + qb), 0, it.kvh * g, tok0);
-          tma_load_3d(qdst + kHalf, &qmap, bar(kBarQFull + qb), 64, it.kvh * g, tok0);
-        } else {
-          mbar_arrive_expect_tx(bar(kBarQFull + qb), kTile);
-          const int row0 = it.q_begin + it.q0;
-          tma_load_3d(qdst, &qmap, bar(kBarQFull + qb), 0, it.h, row0);
-          tma_load_3d(qdst + kHalf, &qmap, bar(kBarQFull + qb), 64, it.h, row0);
+        if (lane == 0) mbar_arrive(bar(kBarQFull));
+      } else {
+        if (lane == 0)
+          mbar_arrive_expect_tx(bar(kBarQFull), kPrefix ? p.rows_per_tile * 256 : kTile);
+        __syncwarp();
+        if (lane >= 2 * kKStages && lane < 2 * kKStages + 2) {   // lanes of their own
+          const int hf = lane & 1;
+          if constexpr (kPrefix) {
+            // (sequence, head) rows of the group: box {64 dims, g heads, tokens}
+            tma_load_3d(qdst + hf * kHalf, &qmap, bar(kBarQFull), hf * 64, it.kvh * g, it.q0 / g);
+          } else {
+            tma_load_3d(qdst + hf * kHalf, &qmap, bar(kBarQFull), hf * 64, it.h,
+                        it.q_begin + it.q0);
+          }
         }
       }
       if (lane == 0) flags[3] = qi + 1;
       __syncwarp();
       return true;
     };
-    // first non-empty item at or after round k
-    auto next_item = [&](int& k, Item& it) -> bool {
-      for (; k < n_rounds; ++k) {
-        const int idx = item_index(k);
-        if (idx >= p.n_items) continue;
-        it = get_item<kPrefix>(p, idx, false);
-        if (it.n > 0) return true;
-      }
-      return false;
-    };
     int k = 0;
     Item it;
-    bool have = next_item(k, it);
-    if (have && !load_q(it, 0)) {
-      ok = false;
-      if (lane == 0) record_error(p.err, kErrTimeout);
-    }
+    bool have = next_item<kPrefix>(p, n_rounds, k, it, false);
     while (have && ok) {
       int k2 = k + 1;
       Item nx;
-      const bool have_next = next_item(k2, nx);
-      const int q_at = min(1, it.n - 1);   // load the next Q after this K tile
+      const bool have_next = next_item<kPrefix>(p, n_rounds, k2, nx, false);
       ids.chunk = -1;
-      for (int kt = 0; kt < it.n; ++kt, ++gk) {
+      for (int kt = 0; kt < it.n; ++kt, ++gk, rk.next()) {
         if (__any_sync(kFull, flags[0] != 0)) { ok = false; break; }
-        const int st = gk & 1;
         const int gkt = it.kt0 + kt;
         const int id = ids.get(it.table, table_limit, gkt >> 1, lane, p.num_blocks, p.err);
         const int slot = id * kBlockSize + (gkt & 1) * kN;
-        if (gk >= 2 && !warp_wait(bar(kBarKEmpty + st), ((gk - 2) >> 1) & 1)) {
+        if (gk >= kKStages && !warp_wait(bar(kBarKEmpty + rk.idx), rk.ph ^ 1u)) {
           ok = false;
           if (lane == 0) record_error(p.err, kErrTimeout);
           break;
         }
         if (lane == 0) {
-          const uint32_t kdst = sbase + kOffK + st * kTile;
-          mbar_arrive_expect_tx(bar(kBarKFull + st), kTile);
-          tma_load_3d(kdst, &kmap, bar(kBarKFull + st), 0, it.kvh, slot);
-          tma_load_3d(kdst + kHalf, &kmap, bar(kBarKFull + st), 64, it.kvh, slot);
+          mbar_arrive_expect_tx(bar(kBarKFull + rk.idx), kTile);
           flags[1] = gk + 1;
         }
         __syncwarp();
-        if (kt == q_at && have_next && !load_q(nx, gi + 1)) {
+        // lanes 2s, 2s+1 load stage s: a lane's next copy never queues behind
+        // its previous one
+        if ((lane >> 1) == rk.idx)
+          tma_load_3d(sbase + kOffK + rk.idx * kTile + (lane & 1) * kHalf, &kmap,
+                      bar(kBarKFull + rk.idx), (lane & 1) * 64, it.kvh, slot);
+        __syncwarp();
+        if (kt == 0 && !load_q(it, gi)) {
           ok = false;
           if (lane == 0) record_error(p.err, kErrTimeout);
           break;
@@ -382,32 +388,38 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
     bool ok = true;
     int gk = 0;
     BlockIds ids;
-    for (int k = 0; k < n_rounds && ok; ++k) {
-      const int idx = item_index(k);
-      if (idx >= p.n_items) continue;
-      const Item it = get_item<kPrefix>(p, idx, false);
-      if (it.n == 0) continue;
+    Ring<kVStages> rv;
+    int k = 0;
+    Item it;
+    bool have = next_item<kPrefix>(p, n_rounds, k, it, false);
+    while (have && ok) {
+      int k2 = k + 1;
+      Item nx;
+      const bool have_next = next_item<kPrefix>(p, n_rounds, k2, nx, false);
       ids.chunk = -1;
-      for (int kt = 0; kt < it.n; ++kt, ++gk) {
+      for (int kt = 0; kt < it.n; ++kt, ++gk, rv.next()) {
         if (__any_sync(kFull, flags[0] != 0)) { ok = false; break; }
-        const int st = gk & 1;
         const int gkt = it.kt0 + kt;
         const int id = ids.get(it.table, table_limit, gkt >> 1, lane, p.num_blocks, p.err);
         const int slot = id * kBlockSize + (gkt & 1) * kN;
-        if (gk >= 2 && !warp_wait(bar(kBarVEmpty + st), ((gk - 2) >> 1) & 1)) {
+        if (gk >= kVStages && !warp_wait(bar(kBarVEmpty + rv.idx), rv.ph ^ 1u)) {
           ok = false;
           if (lane == 0) record_error(p.err, kErrTimeout);
           break;
         }
         if (lane == 0) {
-          const uint32_t vdst = sbase + kOffV + st * kTile;
-          mbar_arrive_expect_tx(bar(kBarVFull + st), kTile);
-          tma_load_3d(vdst, &vmap, bar(kBarVFull + st), 0, it.kvh, slot);
-          tma_load_3d(vdst + kHalf, &vmap, bar(kBarVFull + st), 64, it.kvh, slot);
+          mbar_arrive_expect_tx(bar(kBarVFull + rv.idx), kTile);
           flags[2] = gk + 1;
         }
         __syncwarp();
+        if ((lane >> 1) == rv.idx)
+          tma_load_3d(sbase + kOffV + rv.idx * kTile + (lane & 1) * kHalf, &vmap,
+                      bar(kBarVFull + rv.idx), (lane & 1) * 64, it.kvh, slot);
+        __syncwarp();
       }
+      it = nx;
+      k = k2;
+      have = have_next;
     }
     if (!ok && lane == 0) flags[0] = 1;
   } else if (warp == kSWarp) {
@@ -416,40 +428,44 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
       constexpr uint32_t idesc_s = idesc_bf16_f32(kM, kN, 0);   // B = K, K-major
       bool ok = true, timeout = false;
       int gi = 0, gk = 0;
-      Ring3 sb;
-      for (int k = 0; k < n_rounds && ok; ++k) {
-        const int idx = item_index(k);
-        if (idx >= p.n_items) continue;
-        const Item it = get_item<kPrefix>(p, idx, false);
-        if (it.n == 0) continue;
-        const int qb = gi & 1;
-        if (!mbar_wait(bar(kBarQFull + qb), (gi >> 1) & 1)) { ok = false; timeout = true; break; }
-        const uint32_t q_s = sbase + kOffQ + qb * kTile;
-        for (int kt = 0; kt < it.n; ++kt, ++gk, sb.next()) {
+      Ring<kSBufs> sb;
+      Ring<kKStages> rk;
+      int k = 0;
+      Item it;
+      bool have = next_item<kPrefix>(p, n_rounds, k, it, false);
+      while (have && ok) {
+        int k2 = k + 1;
+        Item nx;
+        const bool have_next = next_item<kPrefix>(p, n_rounds, k2, nx, false);
+        if (!mbar_wait(bar(kBarQFull), gi & 1)) { ok = false; timeout = true; break; }
+        const uint32_t q_s = sbase + kOffQ;
+        for (int kt = 0; kt < it.n; ++kt, ++gk, sb.next(), rk.next()) {
           if (flags[0]) { ok = false; break; }
-          const int st = gk & 1;
-          if (!mbar_wait(bar(kBarKFull + st), (gk >> 1) & 1)) { ok = false; timeout = true; break; }
+          if (!mbar_wait(bar(kBarKFull + rk.idx), rk.ph)) { ok = false; timeout = true; break; }
           // S buffer free: the PV that read P from it (three tiles back) is done
-          if (gk >= kSBufs && !mbar_wait(bar(kBarPVDone + sb.buf), sb.ph ^ 1u)) {
+          if (gk >= kSBufs && !mbar_wait(bar(kBarPVDone + sb.idx), sb.ph ^ 1u)) {
             ok = false;
             timeout = true;
             break;
           }
           tc_fence_after();
-          const uint32_t k_s = sbase + kOffK + st * kTile;
-          const uint32_t d_s = tmem + kColS + sb.buf * kN;
+          const uint32_t k_s = sbase + kOffK + rk.idx * kTile;
+          const uint32_t d_s = tmem + kColS + sb.idx * kN;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
             umma_bf16(d_s, smem_desc_sw128(q_s + off, 16, 1024),
                       smem_desc_sw128(k_s + off, 16, 1024), idesc_s, ks > 0);
           }
-          umma_commit(bar(kBarSFull + sb.buf));
-          umma_commit(bar(kBarKEmpty + st));
+          umma_commit(bar(kBarSFull + sb.idx));
+          umma_commit(bar(kBarKEmpty + rk.idx));
         }
         if (!ok) break;
-        umma_commit(bar(kBarQEmpty + qb));
+        umma_commit(bar(kBarQEmpty));
         ++gi;
+        it = nx;
+        k = k2;
+        have = have_next;
       }
       if (timeout) record_error(p.err, kErrTimeout);
       if (!ok) flags[0] = 1;
@@ -463,25 +479,27 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
       constexpr uint32_t idesc_o = idesc_bf16_f32(kM, kHeadDim, 1);  // B = V, MN-major
       bool ok = true, timeout = false;
       int gk = 0;
-      Ring3 sb;
+      Ring<kSBufs> sb;
+      Ring<kVStages> rv;
       const uint32_t d_o = tmem + kColO;
-      for (int k = 0; k < n_rounds && ok; ++k) {
-        const int idx = item_index(k);
-        if (idx >= p.n_items) continue;
-        const Item it = get_item<kPrefix>(p, idx, false);
-        if (it.n == 0) continue;
-        for (int kt = 0; kt < it.n; ++kt, ++gk, sb.next()) {
+      int k = 0;
+      Item it;
+      bool have = next_item<kPrefix>(p, n_rounds, k, it, false);
+      while (have && ok) {
+        int k2 = k + 1;
+        Item nx;
+        const bool have_next = next_item<kPrefix>(p, n_rounds, k2, nx, false);
+        for (int kt = 0; kt < it.n; ++kt, ++gk, sb.next(), rv.next()) {
           if (flags[0]) { ok = false; break; }
-          const int st = gk & 1;
-          if (!mbar_wait(bar(kBarVFull + st), (gk >> 1) & 1) ||
-              !mbar_wait(bar(kBarPFull + sb.buf), sb.ph)) {
+          if (!mbar_wait(bar(kBarVFull + rv.idx), rv.ph) ||
+              !mbar_wait(bar(kBarPFull + sb.idx), sb.ph)) {
             ok = false;
             timeout = true;
             break;
           }
           tc_fence_after();
-          const uint32_t v_s = sbase + kOffV + st * kTile;
-          const uint32_t p_t = tmem + kColS + sb.buf * kN;
+          const uint32_t v_s = sbase + kOffV + rv.idx * kTile;
+          const uint32_t p_t = tmem + kColS + sb.idx * kN;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             // A = P: 16 keys = 8 packed columns per step.  B = V: 64-dim boxes
@@ -489,11 +507,14 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
             umma_bf16_tmem_a(d_o, p_t + ks * 8, smem_desc_sw128(v_s + ks * 2048, kHalf, 1024),
                              idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
           }
-          umma_commit(bar(kBarVEmpty + st));
-          umma_commit(bar(kBarPVDone + sb.buf));
+          umma_commit(bar(kBarVEmpty + rv.idx));
+          umma_commit(bar(kBarPVDone + sb.idx));
         }
         if (!ok) break;
         umma_commit(bar(kBarOFull));
+        it = nx;
+        k = k2;
+        have = have_next;
       }
       if (timeout) record_error(p.err, kErrTimeout);
       if (!ok) flags[0] = 1;
@@ -502,169 +523,217 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int qd = warp & 3;               // row quarter = TMEM lane quarter
-    const int c = warp >> 2;               // key-column half of every tile
-    const int i = qd * 32 + lane;          // query row within the tile
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(qd * 32) << 16);
-    const uint32_t o_col = lane_base + kColO + c * 64;
+    // Warp w owns 16 whole rows of every tile: TMEM lanes 32(w%4) + 16(w/4) +
+    // [0, 16).  Through the 16x256b access shape thread t holds rows
+    // ra = .. + t/4 and rb = ra + 8, key columns 8k + 2(t%4) + {0, 1}
+    // (k = 0..15); the four threads of a row reduce its max and sum with two
+    // shuffles, and no warp waits for another.
+    const int qd = warp & 3;
+    const int m4 = lane & 3;
+    const int ra = qd * 32 + (warp >> 2) * 16 + (lane >> 2);   // rows within the tile
+    const int rb = ra + 8;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(qd * 32 + (warp >> 2) * 16) << 16);
+    const uint32_t o_col = lane_base + kColO;
     const f32x2 sc2 = pack2(p.scale_log2, p.scale_log2);
     bool ok = true, timeout = false;
     int gi = 0, gk = 0;
-    Ring3 sb;
-    for (int k = 0; k < n_rounds && ok; ++k) {
-      const int idx = item_index(k);
-      if (idx >= p.n_items) continue;
-      const Item it = get_item<kPrefix>(p, idx, warp == 0 && lane == 0);
-      if (it.n == 0) continue;
-      const int vis = it.diag + i;         // last visible key of this row
-      float m = -INFINITY;
-      f32x2 l2 = pack2(0.f, 0.f);          // this half's running sum, as a pair
-      for (int kt = 0; kt < it.n; ++kt, ++gk, sb.next()) {
+    Ring<kSBufs> sb;
+    Ring<kVStages> rv;   // V stage of the current tile (for the ragged-end clearing)
+    auto row_max = [&](float v) {
+      v = fmaxf(v, __shfl_xor_sync(kFull, v, 1));
+      return fmaxf(v, __shfl_xor_sync(kFull, v, 2));
+    };
+    auto row_sum = [&](float v) {
+      v += __shfl_xor_sync(kFull, v, 1);
+      return v + __shfl_xor_sync(kFull, v, 2);
+    };
+    // Output of a finished item: O / l for both rows, written row by row.  It
+    // runs inside the first tile of the next item, after that tile's P is in
+    // place and before P is handed on, so the last PV of the item has long
+    // finished and the next item's first PV cannot overwrite O too early.
+    auto epilogue = [&](const Item& e, float ema, float emb, f32x2 ela, f32x2 elb,
+                        int egi) -> bool {
+      const float la = row_sum(lo2(ela) + hi2(ela));
+      const float lb = row_sum(lo2(elb) + hi2(elb));
+      if (!warp_wait(bar(kBarOFull), egi & 1)) return false;
+      tc_fence_after();
+      const float ia = 1.f / la, ib = 1.f / lb;
+      const bool va = ra < e.rows, vb = rb < e.rows;
+      int64_t rowa = 0, rowb = 0;   // output rows (causal) or partial rows (shared prefix)
+      if constexpr (kPrefix) {
+        const int ga = e.q0 + ra, gb = e.q0 + rb;
+        rowa = (static_cast<int64_t>(ga / g) * p.Hq + e.kvh * g + ga % g) * p.splits + e.z;
+        rowb = (static_cast<int64_t>(gb / g) * p.Hq + e.kvh * g + gb % g) * p.splits + e.z;
+      } else {
+        rowa = static_cast<int64_t>(e.q_begin + e.q0 + ra) * p.Hq + e.h;
+        rowb = static_cast<int64_t>(e.q_begin + e.q0 + rb) * p.Hq + e.h;
+      }
+#pragma unroll 1
+      for (int h2 = 0; h2 < 2; ++h2) {   // dims [64 h2, 64 h2 + 64): box h2 of the row
+        uint32_t o[32];
+        tmem_ld16x256_x8_wait(o_col + h2 * 64, o);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int col = 64 * h2 + 8 * j + 2 * m4;
+          const float a0 = __uint_as_float(o[4 * j]) * ia, a1 = __uint_as_float(o[4 * j + 1]) * ia;
+          const float b0 = __uint_as_float(o[4 * j + 2]) * ib, b1 = __uint_as_float(o[4 * j + 3]) * ib;
+          if constexpr (kPrefix) {
+            if (va) *reinterpret_cast<float2*>(p.part_o + rowa * kHeadDim + col) = make_float2(a0, a1);
+            if (vb) *reinterpret_cast<float2*>(p.part_o + rowb * kHeadDim + col) = make_float2(b0, b1);
+          } else {
+            if (va) *reinterpret_cast<uint32_t*>(p.out + rowa * kHeadDim + col) = pack_bf16x2(a0, a1);
+            if (vb) *reinterpret_cast<uint32_t*>(p.out + rowb * kHeadDim + col) = pack_bf16x2(b0, b1);
+          }
+        }
+      }
+      if (m4 == 0) {
+        if constexpr (kPrefix) {
+          if (va) p.part_lse[rowa] = ema + __log2f(la);
+          if (vb) p.part_lse[rowb] = emb + __log2f(lb);
+        } else if (p.lse) {
+          if (va) p.lse[rowa] = (ema + __log2f(la)) * kLn2;
+          if (vb) p.lse[rowb] = (emb + __log2f(lb)) * kLn2;
+        }
+      }
+      return true;
+    };
+    bool pend = false;        // an item's output is still to be written
+    Item pit;
+    float pma = 0.f, pmb = 0.f;
+    f32x2 pla = 0ull, plb = 0ull;
+    int k = 0;
+    Item it;
+    bool have = next_item<kPrefix>(p, n_rounds, k, it, warp == 0 && lane == 0);
+    while (have && ok) {
+      int k2 = k + 1;
+      Item nx;
+      const bool have_next = next_item<kPrefix>(p, n_rounds, k2, nx, warp == 0 && lane == 0);
+      const int visa = it.diag + ra, visb = it.diag + rb;   // last visible keys
+      float ma = -INFINITY, mb = -INFINITY;
+      f32x2 la2 = pack2(0.f, 0.f), lb2 = pack2(0.f, 0.f);  // running sums, as pairs
+      for (int kt = 0; kt < it.n; ++kt, ++gk, sb.next(), rv.next()) {
         if (__any_sync(kFull, flags[0] != 0)) { ok = false; break; }
-        const uint32_t s_col = lane_base + kColS + sb.buf * kN;
-        if (!(ok = warp_wait(bar(kBarSFull + sb.buf), sb.ph))) { timeout = true; break; }
+        const uint32_t s_col = lane_base + kColS + sb.idx * kN;
+        if (!(ok = warp_wait(bar(kBarSFull + sb.idx), sb.ph))) { timeout = true; break; }
         tc_fence_after();
         uint32_t r[64];
-        tmem_ld64_wait(s_col + c * 64, r);
-        const int j0 = (it.kt0 + kt) * kN + c * 64;   // key of column 0 of this half
-        if (!kPrefix && j0 + 63 > it.diag) {          // causal edge: hide later keys
+        tmem_ld16x256_x16_wait(s_col, r);
+        const int j0 = (it.kt0 + kt) * kN + 2 * m4;   // key of register 0
+        if (!kPrefix && (it.kt0 + kt) * kN + kN - 1 > it.diag) {   // causal edge
 #pragma unroll
-          for (int cc = 0; cc < 64; ++cc)
-            if (j0 + cc > vis) r[cc] = __float_as_uint(-INFINITY);
+          for (int q = 0; q < 16; ++q) {
+            const int key = j0 + 8 * q;
+            if (key > visa) r[4 * q] = __float_as_uint(-INFINITY);
+            if (key + 1 > visa) r[4 * q + 1] = __float_as_uint(-INFINITY);
+            if (key > visb) r[4 * q + 2] = __float_as_uint(-INFINITY);
+            if (key + 1 > visb) r[4 * q + 3] = __float_as_uint(-INFINITY);
+          }
         }
-        float mx[8];
+        float xa0 = __uint_as_float(r[0]), xa1 = __uint_as_float(r[1]);
+        float xb0 = __uint_as_float(r[2]), xb1 = __uint_as_float(r[3]);
 #pragma unroll
-        for (int t = 0; t < 8; ++t) mx[t] = __uint_as_float(r[t]);
-#pragma unroll
-        for (int cc = 8; cc < 64; ++cc) mx[cc & 7] = fmaxf(mx[cc & 7], __uint_as_float(r[cc]));
-        const float pm = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-        // exchange the partial maxima of the two halves of these rows
-        float* xm = xmax + (gk & 1) * 256;
-        xm[c * 128 + i] = pm;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarXMax + qd * 2 + (gk & 1)));
-        if (!(ok = warp_wait(bar(kBarXMax + qd * 2 + (gk & 1)), (gk >> 1) & 1))) {
-          timeout = true;
-          break;
+        for (int q = 1; q < 16; ++q) {
+          xa0 = fmaxf(xa0, __uint_as_float(r[4 * q]));
+          xa1 = fmaxf(xa1, __uint_as_float(r[4 * q + 1]));
+          xb0 = fmaxf(xb0, __uint_as_float(r[4 * q + 2]));
+          xb1 = fmaxf(xb1, __uint_as_float(r[4 * q + 3]));
         }
-        // both halves have read their S columns: P may now overwrite them
-        const float mt = fmaxf(pm, xm[(c ^ 1) * 128 + i]) * p.scale_log2;
+        const float mta = row_max(fmaxf(xa0, xa1)) * p.scale_log2;
+        const float mtb = row_max(fmaxf(xb0, xb1)) * p.scale_log2;
         if (kt == 0) {
-          m = mt;
+          ma = mta;
+          mb = mtb;
         } else {
-          const bool need = mt > m + kLazyRescale;
-          if (__any_sync(kFull, need)) {
+          const bool need_a = mta > ma + kLazyRescale, need_b = mtb > mb + kLazyRescale;
+          if (__any_sync(kFull, need_a || need_b)) {
             // the previous PV must have finished accumulating into O
-            const int pb = sb.buf == 0 ? kSBufs - 1 : sb.buf - 1;
-            const uint32_t pph = sb.buf == 0 ? sb.ph ^ 1u : sb.ph;
+            const int pb = sb.idx == 0 ? kSBufs - 1 : sb.idx - 1;
+            const uint32_t pph = sb.idx == 0 ? sb.ph ^ 1u : sb.ph;
             if (!(ok = warp_wait(bar(kBarPVDone + pb), pph))) { timeout = true; break; }
             tc_fence_after();
-            const float alpha = need ? ex2(m - mt) : 1.f;
-            if (need) {
-              l2 = mul2(l2, pack2(alpha, alpha));
-              m = mt;
+            const float alpha_a = need_a ? ex2(ma - mta) : 1.f;
+            const float alpha_b = need_b ? ex2(mb - mtb) : 1.f;
+            if (need_a) {
+              la2 = mul2(la2, pack2(alpha_a, alpha_a));
+              ma = mta;
+            }
+            if (need_b) {
+              lb2 = mul2(lb2, pack2(alpha_b, alpha_b));
+              mb = mtb;
             }
 #pragma unroll 1
-            for (int hh = 0; hh < 2; ++hh) {
+            for (int h2 = 0; h2 < 2; ++h2) {
               uint32_t o[32];
-              tmem_ld32_wait(o_col + hh * 32, o);
+              tmem_ld16x256_x8_wait(o_col + h2 * 64, o);
 #pragma unroll
-              for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
-              tmem_st32(o_col + hh * 32, o);
+              for (int j = 0; j < 8; ++j) {
+                o[4 * j] = __float_as_uint(__uint_as_float(o[4 * j]) * alpha_a);
+                o[4 * j + 1] = __float_as_uint(__uint_as_float(o[4 * j + 1]) * alpha_a);
+                o[4 * j + 2] = __float_as_uint(__uint_as_float(o[4 * j + 2]) * alpha_b);
+                o[4 * j + 3] = __float_as_uint(__uint_as_float(o[4 * j + 3]) * alpha_b);
+              }
+              tmem_st16x256_x8(o_col + h2 * 64, o);
             }
           }
         }
-        // P = 2^(scale*s - m) as bf16 pairs: columns [32c, 32c+32) of the S buffer.
-        // Hidden keys hold -inf, so their weight is exactly 0.
-        const f32x2 nm2 = pack2(-m, -m);
+        // P = 2^(scale*s - m) as bf16 pairs: P column 4q + m4 holds keys
+        // 8q + 2 m4 + {0, 1} (the 16x128b shape).  Hidden keys hold -inf and
+        // get weight exactly 0.
+        const f32x2 nma = pack2(-ma, -ma), nmb = pack2(-mb, -mb);
         uint32_t pk[32];
-        f32x2 acc0 = pack2(0.f, 0.f), acc1 = pack2(0.f, 0.f);
+        f32x2 sa = pack2(0.f, 0.f), sb2 = pack2(0.f, 0.f);
 #pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          const f32x2 x =
-              fma2(pack2(__uint_as_float(r[2 * t]), __uint_as_float(r[2 * t + 1])), sc2, nm2);
-          const float e0 = ex2(lo2(x)), e1 = ex2(hi2(x));
-          pk[t] = pack_bf16x2(e0, e1);
-          if (t & 1)
-            acc1 = add2(acc1, pack2(e0, e1));
-          else
-            acc0 = add2(acc0, pack2(e0, e1));
+        for (int q = 0; q < 16; ++q) {
+          const f32x2 xa =
+              fma2(pack2(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1])), sc2, nma);
+          const f32x2 xb =
+              fma2(pack2(__uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])), sc2, nmb);
+          const float a0 = ex2(lo2(xa)), a1 = ex2(hi2(xa));
+          const float b0 = ex2(lo2(xb)), b1 = ex2(hi2(xb));
+          pk[2 * q] = pack_bf16x2(a0, a1);
+          pk[2 * q + 1] = pack_bf16x2(b0, b1);
+          sa = add2(sa, pack2(a0, a1));
+          sb2 = add2(sb2, pack2(b0, b1));
         }
-        l2 = add2(l2, add2(acc0, acc1));
-        tmem_st32(s_col + c * 32, pk);
+        la2 = add2(la2, sa);
+        lb2 = add2(lb2, sb2);
+        tmem_st16x128_x16(s_col, pk);
         // keys past the end of the sequence in its last tile: zero their V rows
-        // so that 0 * (stale data) cannot put a NaN into O
+        // so that 0 * (stale data) cannot put a NaN into O (thread s of the 256
+        // softmax threads clears row s/2, dims 64(s%2)..)
         if (!kPrefix && kt == it.n - 1 && (it.kt0 + kt) * kN + kN > it.Lk) {
-          const int st = gk & 1;
-          if (!(ok = warp_wait(bar(kBarVFull + st), (gk >> 1) & 1))) { timeout = true; break; }
-          if ((it.kt0 + kt) * kN + i >= it.Lk) {
+          if (!(ok = warp_wait(bar(kBarVFull + rv.idx), rv.ph))) { timeout = true; break; }
+          const int vr = tid >> 1, vh = tid & 1;
+          if ((it.kt0 + kt) * kN + vr >= it.Lk) {
             const uint4 zero = make_uint4(0, 0, 0, 0);
-            const uint32_t vrow = sbase + kOffV + st * kTile + c * kHalf + i * 128;
+            const uint32_t vrow = sbase + kOffV + rv.idx * kTile + vh * kHalf + vr * 128;
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) sts128(vrow + cc * 16, zero);
           }
           fence_proxy_async_smem();
         }
         tmem_wait_st();
+        if (kt == 0 && pend) {
+          pend = false;
+          if (!(ok = epilogue(pit, pma, pmb, pla, plb, gi - 1))) { timeout = true; break; }
+        }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarPFull + sb.buf));
+        if (lane == 0) mbar_arrive(bar(kBarPFull + sb.idx));
       }
       if (!ok) break;
-      // ---- epilogue: row sum of both halves, O / l, out and lse
-      float lsum = lo2(l2) + hi2(l2);
-      xsum[c * 128 + i] = lsum;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarXSum + qd));
-      if (!(ok = warp_wait(bar(kBarXSum + qd), gi & 1))) { timeout = true; break; }
-      lsum += xsum[(c ^ 1) * 128 + i];
-      if (!(ok = warp_wait(bar(kBarOFull), gi & 1))) { timeout = true; break; }
-      tc_fence_after();
-      const float inv = 1.f / lsum;
-      const bool valid = i < it.rows;
-      int64_t row = 0;
-      if constexpr (kPrefix) {
-        const int gr = it.q0 + i;
-        row = static_cast<int64_t>(gr / g) * p.Hq + it.kvh * g + gr % g;
-        row = row * p.splits + it.z;
-      } else {
-        row = static_cast<int64_t>(it.q_begin + it.q0 + i) * p.Hq + it.h;
-      }
-#pragma unroll 1
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t o[32];
-        tmem_ld32_wait(o_col + hh * 32, o);
-        if (!valid) continue;
-        if constexpr (kPrefix) {
-          float4* dst = reinterpret_cast<float4*>(p.part_o + row * kHeadDim + c * 64 + hh * 32);
-#pragma unroll
-          for (int t = 0; t < 8; ++t)
-            dst[t] = make_float4(__uint_as_float(o[4 * t]) * inv, __uint_as_float(o[4 * t + 1]) * inv,
-                                 __uint_as_float(o[4 * t + 2]) * inv,
-                                 __uint_as_float(o[4 * t + 3]) * inv);
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + row * kHeadDim + c * 64 + hh * 32);
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[8 * t + 0]) * inv, __uint_as_float(o[8 * t + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(o[8 * t + 2]) * inv, __uint_as_float(o[8 * t + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(o[8 * t + 4]) * inv, __uint_as_float(o[8 * t + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(o[8 * t + 6]) * inv, __uint_as_float(o[8 * t + 7]) * inv);
-            dst[t] = v;
-          }
-        }
-      }
-      if (valid && c == 0) {
-        if constexpr (kPrefix) {
-          p.part_lse[row] = m + __log2f(lsum);
-        } else {
-          if (p.lse) p.lse[row] = (m + __log2f(lsum)) * kLn2;
-        }
-      }
+      pend = true;
+      pit = it;
+      pma = ma;
+      pmb = mb;
+      pla = la2;
+      plb = lb2;
       ++gi;
+      it = nx;
+      k = k2;
+      have = have_next;
     }
+    if (ok && pend && !(ok = epilogue(pit, pma, pmb, pla, plb, gi - 1))) timeout = true;
     if (timeout && lane == 0) record_error(p.err, kErrTimeout);
     if (!ok && lane == 0) flags[0] = 1;
   }
@@ -675,15 +744,14 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
   // the last two issued tiles of each ring.
   if (flags[0] && tid == kQKWarp * 32) {
     const int kin = flags[1], qin = flags[3];
-    for (int x = max(0, kin - 2); x < kin; ++x)
-      (void)mbar_wait(bar(kBarKFull + (x & 1)), (x >> 1) & 1);
-    for (int x = max(0, qin - 2); x < qin; ++x)
-      (void)mbar_wait(bar(kBarQFull + (x & 1)), (x >> 1) & 1);
+    for (int x = max(0, kin - kKStages); x < kin; ++x)
+      (void)mbar_wait(bar(kBarKFull + x % kKStages), (x / kKStages) & 1);
+    if (qin > 0) (void)mbar_wait(bar(kBarQFull), (qin - 1) & 1);
   }
   if (flags[0] && tid == kVWarp * 32) {
     const int vin = flags[2];
-    for (int x = max(0, vin - 2); x < vin; ++x)
-      (void)mbar_wait(bar(kBarVFull + (x & 1)), (x >> 1) & 1);
+    for (int x = max(0, vin - kVStages); x < vin; ++x)
+      (void)mbar_wait(bar(kBarVFull + x % kVStages), (x / kVStages) & 1);
   }
   __syncthreads();
   if (warp == kSWarp) {
@@ -751,8 +819,8 @@ int launch_prefill(const PrefillArgs& a, unsigned* err, cudaStream_t stream) {
   prm.num_blocks = a.num_blocks;
   prm.scale_log2 = a.scale * 1.4426950408889634f;
   if (!set_smem_attr<false>()) return PKV_ERR_LAUNCH;
-  paged_prefill_kernel<false><<<grid_for(prm.n_items), kThreads, kSmemBytes, stream>>>(qm, km, vm,
-                                                                                       prm);
+  paged_prefill_kernel<false><<<grid_for(prm.n_items), kThreads, kSmemBytes, stream>>>(
+      qm, km, vm, prm);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }
 
@@ -788,8 +856,8 @@ int launch_prefix_attention(const PrefixArgs& a, unsigned* err, cudaStream_t str
   if (items > INT32_MAX) return PKV_ERR_SHAPE;
   prm.n_items = static_cast<int>(items);
   if (!set_smem_attr<true>()) return PKV_ERR_LAUNCH;
-  paged_prefill_kernel<true><<<grid_for(prm.n_items), kThreads, kSmemBytes, stream>>>(qm, km, vm,
-                                                                                      prm);
+  paged_prefill_kernel<true><<<grid_for(prm.n_items), kThreads, kSmemBytes, stream>>>(
+      qm, km, vm, prm);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }
 
