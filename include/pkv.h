@@ -229,6 +229,35 @@ int paged_decode_attention_noalloc(void* out, float* lse, const void* q,
                                    int D, int block_size, int64_t num_blocks, float scale,
                                    int num_splits, pkv_stream_t stream);
 
+/* paged_decode_attention_multiquery — decode attention for q_len new tokens
+ * per sequence at once: the check of a speculator's proposed tokens in
+ * speculative decoding, which turns sequential decode into a parallel
+ * "mini-prefill" ("What Is an Inference Engine, Anyway?", Technical details,
+ * Speculative Decoding).  Same operation as paged_prefill_attention with
+ * Lq = q_len and Lk = context_lens[b] for every sequence, computed by the
+ * split-K decode kernel (memory bound, like decode) instead of 128-row tensor
+ * core tiles.
+ * q   : bf16 [B, q_len, Hq, D] contiguous.   out : bf16 [B, q_len, Hq, D].
+ * lse : f32 [B, q_len, Hq] (natural log) or NULL.
+ * context_lens[b] counts every cached token of sequence b, its q_len new ones
+ * included (they must already be stored); position i (0 <= i < q_len) sees
+ * keys j < context_lens[b] - q_len + 1 + i.
+ * 1 <= q_len <= 64.  Other arguments, the workspace rules (size from
+ * paged_decode_multiquery_workspace_bytes) and the errors are those of
+ * paged_decode_attention; context_lens[b] < q_len is reported as
+ * PKV_ERR_DEVICE_INDEX through pkv_get_device_error().  q_len = 1 is exactly
+ * paged_decode_attention. */
+size_t paged_decode_multiquery_workspace_bytes(int B, int q_len, int Hq, int Hkv, int D,
+                                               int max_blocks_per_seq, int block_size,
+                                               int num_splits);
+int paged_decode_attention_multiquery(void* out, float* lse, const void* q,
+                                      const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, int max_blocks_per_seq,
+                                      const int32_t* context_lens, int B, int q_len, int Hq,
+                                      int Hkv, int D, int block_size, int64_t num_blocks,
+                                      float scale, void* workspace, size_t workspace_bytes,
+                                      int num_splits, pkv_stream_t stream);
+
 /* paged_prefill_attention — causal prefill / chunked prefill with a prefix
  * cache: "During prefill with prefix cache, gathers cached K/V from the paged
  * cache and concatenates with newly computed ones" (Nano-vLLM System

@@ -188,6 +188,53 @@ extern "C" int paged_decode_attention(void* out, float* lse, const void* q, cons
   return launch_decode(a, plan, err, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// Longest run of query positions per sequence the multi-query decode accepts.
+constexpr int kMaxQueryLen = 64;
+
+extern "C" size_t paged_decode_multiquery_workspace_bytes(int B, int q_len, int Hq, int Hkv,
+                                                          int D, int max_blocks_per_seq,
+                                                          int block_size, int num_splits) {
+  if (D != kHeadDim || block_size != kBlockSize || num_splits < 0) return 0;
+  if (q_len < 1 || q_len > kMaxQueryLen) return 0;
+  DecodePlan plan;
+  if (plan_decode(B, Hq * q_len, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), 0,
+                  &plan))
+    return 0;
+  return plan.workspace_bytes;
+}
+
+extern "C" int paged_decode_attention_multiquery(
+    void* out, float* lse, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens, int B,
+    int q_len, int Hq, int Hkv, int D, int block_size, int64_t num_blocks, float scale,
+    void* workspace, size_t workspace_bytes, int num_splits, pkv_stream_t stream) {
+  if (B < 0 || Hq <= 0 || max_blocks_per_seq < 0 || num_splits < 0) return PKV_ERR_ARG;
+  if (q_len < 1 || q_len > kMaxQueryLen) return PKV_ERR_ARG;
+  int st = check_pool(Hkv, D, block_size, num_blocks);
+  if (st) return st;
+  if (Hq % Hkv) return PKV_ERR_SHAPE;
+  if (B == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !context_lens) return PKV_ERR_ARG;
+  if (max_blocks_per_seq > 0 && !block_tables) return PKV_ERR_ARG;
+  if (num_blocks == 0 && max_blocks_per_seq > 0) return PKV_ERR_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_ARG;
+  DecodePlan plan;
+  st = plan_decode(B, Hq * q_len, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), 0,
+                   &plan);
+  if (st) return st;
+  if (plan.workspace_bytes) {
+    if (!workspace || workspace_bytes < plan.workspace_bytes ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+      return PKV_ERR_WORKSPACE;
+  }
+  unsigned* err = device_error_word();
+  if (!err) return PKV_ERR_LAUNCH;
+  DecodeArgs a{out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+               B, Hq, Hkv, num_blocks, scale, workspace, workspace_bytes, num_splits, 0, q_len};
+  return launch_decode(a, plan, err, reinterpret_cast<cudaStream_t>(stream));
+}
+
 namespace {
 
 int check_shared_prefix(int max_blocks_per_seq, int shared_prefix_tokens) {

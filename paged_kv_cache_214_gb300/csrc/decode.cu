@@ -70,7 +70,11 @@ struct DecodeParams {
   float* ws_lse;      // [B*Hq, S] partial log2-sum-exp
   unsigned* ws_count; // [B * Hkv * head_groups] arrival counters
   unsigned* err;
+  // Hq counts "virtual" heads: q_len query positions x the physical heads;
+  // virtual head v of kv head kv is position (v%g)/(g/q_len), head
+  // kv*(g/q_len) + (v%g)%(g/q_len), with g = Hq/Hkv.  q_len = 1 is plain decode.
   int B, Hq, Hkv, maxblk, num_splits, split_blocks, head_groups;
+  int q_len, Hq_phys;
   int64_t num_blocks;
   float scale_log2;
   // Shared prefix (0 = none): every sequence's first prefix_tokens tokens are
@@ -187,6 +191,21 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     if (tid == 0 && split == 0 && hg == 0) record_error(p.err, kErrIndex);
     ctx = ctx < P ? P : cap;
   }
+  // several query positions: every one of the q_len new tokens is in the cache
+  if (p.q_len > 1 && ctx < p.q_len && tid == 0 && split == 0 && hg == 0)
+    record_error(p.err, kErrIndex);
+  // row of q / out / lse for virtual head v, and the number of keys it sees
+  // (position i of q_len sees keys j < ctx - q_len + 1 + i)
+  const int gp = g / p.q_len;
+  auto phys_row = [&](int v) -> int64_t {
+    if (p.q_len == 1) return static_cast<int64_t>(b) * p.Hq + v;
+    const int kv = v / g, r = v - kv * g;
+    return (static_cast<int64_t>(b) * p.q_len + r / gp) * p.Hq_phys + kv * gp + r % gp;
+  };
+  auto key_limit = [&](int v) -> int {
+    if (p.q_len == 1) return ctx;
+    return ctx - (p.q_len - 1 - (v % g) / gp);
+  };
   const int nsplit = (ctx - P + split_tokens - 1) / split_tokens;
   if (split >= (nsplit > 0 ? nsplit : 1)) return;  // whole block exits: no work
 
@@ -203,18 +222,17 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       for (int r = warp; r < KVH * G; r += kConsumerWarps) {
         const int64_t row = static_cast<int64_t>(b) * p.Hq + qhead(r / G, r % G);
         const int np = p.prefix_splits;
+        const int64_t prow = phys_row(qhead(r / G, r % G));
         merge_row(nullptr, nullptr, 0, p.prefix_lse + row * np, p.prefix_o + row * np * kHeadDim,
-                  np, p.out + row * kHeadDim, p.lse ? p.lse + row : nullptr, lane);
+                  np, p.out + prow * kHeadDim, p.lse ? p.lse + prow : nullptr, lane);
       }
       return;
     }
     for (int i = tid; i < KVH * G * kHeadDim; i += kThreads) {
       const int r = i / kHeadDim, d = i % kHeadDim;
-      p.out[(static_cast<int64_t>(b) * p.Hq + qhead(r / G, r % G)) * kHeadDim + d] =
-          __float2bfloat16_rn(0.f);
+      p.out[phys_row(qhead(r / G, r % G)) * kHeadDim + d] = __float2bfloat16_rn(0.f);
     }
-    if (p.lse && tid < KVH * G)
-      p.lse[static_cast<int64_t>(b) * p.Hq + qhead(tid / G, tid % G)] = -INFINITY;
+    if (p.lse && tid < KVH * G) p.lse[phys_row(qhead(tid / G, tid % G))] = -INFINITY;
     return;
   }
 
@@ -280,8 +298,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     f32x2 q2[G][8];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const __nv_bfloat16* qp =
-          p.q + (static_cast<int64_t>(b) * p.Hq + qhead(my_hh, h)) * kHeadDim;
+      const __nv_bfloat16* qp = p.q + phys_row(qhead(my_hh, h)) * kHeadDim;
       const uint4 a = __ldg(reinterpret_cast<const uint4*>(qp + 8 * j));
       const uint4 c = __ldg(reinterpret_cast<const uint4*>(qp + 64 + 8 * j));
       const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
@@ -291,10 +308,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     }
     f32x2 o2[G][8];
     float m[G], l[G];
+    int lim[G];   // keys of this split visible to head h: tile-relative index < lim
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       m[h] = -INFINITY;
       l[h] = 0.f;
+      lim[h] = key_limit(qhead(my_hh, h)) - tok_begin;
 #pragma unroll
       for (int i = 0; i < 8; ++i) o2[h][i] = 0ull;
     }
@@ -338,7 +357,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
           acc += __shfl_xor_sync(0xffffffffu, acc, 1);
           acc += __shfl_xor_sync(0xffffffffu, acc, 2);
           acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-          sc[r][h] = t < n_valid ? acc : -INFINITY;
+          sc[r][h] = (t < n_valid && it * kTT + t < lim[h]) ? acc : -INFINITY;
         }
       }
       // online softmax, once per tile.  The running max only moves when the
@@ -358,7 +377,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const int t = 4 * (r * kWPH + my_wl) + grp;
-          sc[r][h] = t < n_valid ? ex2(sc[r][h] - m[h]) : 0.f;
+          sc[r][h] = (t < n_valid && it * kTT + t < lim[h]) ? ex2(sc[r][h] - m[h]) : 0.f;
           l[h] += sc[r][h];
         }
       }
@@ -468,12 +487,15 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       Ls += merge_l[w * G + h] * c;
       Os += merge_o[(w * G + h) * kHeadDim + d] * c;
     }
-    const float on = Os / Ls;
+    // a split may hold no key a row can see (later query positions only):
+    // its partial is then 0 with log2-sum-exp -inf, which the merge ignores
+    const float on = Ls > 0.f ? Os / Ls : 0.f;
     const float lse2 = M + __log2f(Ls);
     const int64_t row = static_cast<int64_t>(b) * p.Hq + qhead(hh, h);
     if (single) {
-      p.out[row * kHeadDim + d] = __float2bfloat16_rn(on);
-      if (p.lse && d == 0) p.lse[row] = lse2 * kLn2;
+      const int64_t orow = phys_row(qhead(hh, h));
+      p.out[orow * kHeadDim + d] = __float2bfloat16_rn(on);
+      if (p.lse && d == 0) p.lse[orow] = lse2 * kLn2;
     } else {
       const int64_t prow = row * p.num_splits + split;
       __stcg(p.ws_o + prow * kHeadDim + d, on);
@@ -498,11 +520,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   if (!flags[1]) return;
   for (int r = warp; r < KVH * G; r += kConsumerWarps) {
     const int64_t row = static_cast<int64_t>(b) * p.Hq + qhead(r / G, r % G);
+    const int64_t orow = phys_row(qhead(r / G, r % G));
     const int np = P > 0 ? p.prefix_splits : 0;
     merge_row(p.ws_lse + row * p.num_splits, p.ws_o + row * p.num_splits * kHeadDim, nsplit,
               np ? p.prefix_lse + row * np : nullptr,
-              np ? p.prefix_o + row * np * kHeadDim : nullptr, np, p.out + row * kHeadDim,
-              p.lse ? p.lse + row : nullptr, lane);
+              np ? p.prefix_o + row * np * kHeadDim : nullptr, np, p.out + orow * kHeadDim,
+              p.lse ? p.lse + orow : nullptr, lane);
   }
   if (tid == 0) *counter = 0u;  // ready for the next call
 }
@@ -619,7 +642,9 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
   prm.context_lens = a.context_lens;
   prm.err = err;
   prm.B = a.B;
-  prm.Hq = a.Hq;
+  prm.Hq = a.Hq * a.q_len;   // virtual heads (see DecodeParams)
+  prm.Hq_phys = a.Hq;
+  prm.q_len = a.q_len;
   prm.Hkv = a.Hkv;
   prm.maxblk = a.max_blocks_per_seq;
   prm.num_splits = plan.num_splits;
@@ -639,7 +664,7 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
                             sizeof(float), 256));
   }
   if (plan.workspace_bytes > 0) {
-    const size_t rows = static_cast<size_t>(a.B) * a.Hq * plan.num_splits;
+    const size_t rows = static_cast<size_t>(a.B) * a.Hq * a.q_len * plan.num_splits;
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     prm.ws_count = reinterpret_cast<unsigned*>(ws);
     ws += kCounterRegion;

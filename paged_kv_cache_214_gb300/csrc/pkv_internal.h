@@ -62,6 +62,7 @@ struct DecodeArgs {
   size_t workspace_bytes;
   int num_splits;  // as requested (0 = automatic)
   int prefix_tokens;  // shared prefix handled by a separate pass (0 = none)
+  int q_len = 1;      // query positions per sequence (several: speculative verify)
 };
 
 // Split plan of one decode call.

@@ -71,6 +71,11 @@ def load_library(path: str = LIB_PATH):
         lib.paged_decode_attention_noalloc.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32,
                                                        i32, i32, i64, f32, i32, P]
         lib.paged_decode_attention_noalloc.restype = i32
+        lib.paged_decode_multiquery_workspace_bytes.argtypes = [i32] * 8
+        lib.paged_decode_multiquery_workspace_bytes.restype = sz
+        lib.paged_decode_attention_multiquery.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32,
+                                                          i32, i32, i32, i64, f32, P, sz, i32, P]
+        lib.paged_decode_attention_multiquery.restype = i32
         lib.paged_prefill_attention.argtypes = [P, P, P, P, P, P, i32, P, P, i32, i32, i32,
                                                 i32, i32, i32, i32, i64, f32, P]
         lib.paged_prefill_attention.restype = i32
@@ -225,6 +230,53 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                                       _ptr(context_lens), B, Hq, Hkv, D, bs, NB, float(scale),
                                       _ptr(workspace), ws_bytes, int(num_splits),
                                       _stream(stream)), "paged_decode_attention")
+    return out, lse
+
+
+def paged_decode_multiquery_workspace_bytes(B: int, q_len: int, Hq: int, Hkv: int, D: int,
+                                            max_blocks_per_seq: int, block_size: int = 256,
+                                            num_splits: int = 0) -> int:
+    return int(load_library().paged_decode_multiquery_workspace_bytes(
+        B, q_len, Hq, Hkv, D, max_blocks_per_seq, block_size, num_splits))
+
+
+def paged_decode_attention_multiquery(q: torch.Tensor, k_cache: torch.Tensor,
+                                      v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                      context_lens: torch.Tensor, scale: float,
+                                      out: Optional[torch.Tensor] = None,
+                                      lse: Optional[torch.Tensor] = None,
+                                      workspace: Optional[torch.Tensor] = None,
+                                      num_splits: int = 0, want_lse: bool = True, stream=None
+                                      ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """q bf16 [B, q_len, Hq, D]: q_len new positions per sequence (already stored
+    in the cache, counted in context_lens).  Returns (out bf16 [B, q_len, Hq, D],
+    lse fp32 [B, q_len, Hq] or None)."""
+    lib = load_library()
+    NB, bs, Hkv, D = _pool_dims(k_cache, v_cache)
+    _need(q, "q", torch.bfloat16, 4)
+    B, q_len, Hq, Dq = q.shape
+    if Dq != D:
+        raise ValueError("q head_dim differs from the cache's")
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables / context_lens batch differs from q")
+    maxblk = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 4)
+    if lse is None and want_lse:
+        lse = torch.empty((B, q_len, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+    need = paged_decode_multiquery_workspace_bytes(B, q_len, Hq, Hkv, D, maxblk, bs, num_splits)
+    if workspace is None and need:
+        workspace = decode_workspace(need, q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.paged_decode_attention_multiquery(
+        _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), maxblk,
+        _ptr(context_lens), B, q_len, Hq, Hkv, D, bs, NB, float(scale), _ptr(workspace), ws_bytes,
+        int(num_splits), _stream(stream)), "paged_decode_attention_multiquery")
     return out, lse
 
 

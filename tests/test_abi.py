@@ -59,6 +59,24 @@ def test_host_argument_checks(lib):
     assert lib.kv_cache_store(None, None, 0, 0, None, None, None, 0, 8, 128, 256, 1 << 24, s) == pkv.PKV_ERR_SHAPE
 
 
+def test_multiquery_host_checks(lib):
+    s = None
+    mq = lib.paged_decode_attention_multiquery
+    # q_len outside [1, 64]
+    assert mq(None, None, None, None, None, None, 1, None, 2, 0, 16, 8, 128, 256, 16, 1.0,
+              None, 0, 0, s) == pkv.PKV_ERR_ARG
+    assert mq(None, None, None, None, None, None, 1, None, 2, 65, 16, 8, 128, 256, 16, 1.0,
+              None, 0, 0, s) == pkv.PKV_ERR_ARG
+    # Hq not a multiple of Hkv, empty batch, missing pointers
+    assert mq(None, None, None, None, None, None, 1, None, 2, 4, 12, 8, 128, 256, 16, 1.0,
+              None, 0, 0, s) == pkv.PKV_ERR_SHAPE
+    assert mq(None, None, None, None, None, None, 1, None, 0, 4, 16, 8, 128, 256, 16, 1.0,
+              None, 0, 0, s) == pkv.PKV_OK
+    assert mq(None, None, None, None, None, None, 1, None, 2, 4, 16, 8, 128, 256, 16, 1.0,
+              None, 0, 0, s) == pkv.PKV_ERR_ARG
+    assert lib.paged_decode_multiquery_workspace_bytes(2, 0, 16, 8, 128, 4, 256, 0) == 0
+
+
 def test_workspace_query_and_split_plan(lib):
     # one split needs no workspace; several need partials + counters
     assert pkv.paged_decode_workspace_bytes(4, 16, 8, 128, 1, 256, 1) == 0
