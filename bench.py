@@ -575,7 +575,62 @@ def run_extras(pkv, dev, hbm_peak, args):
     except Exception as e:  # reported, not hidden
         entry["prefill_error"] = str(e)
     res[w.name] = entry
+    del w, q, kc, vc, kn, vn, slots, tables, cq, ck, out, lse
+    torch.cuda.empty_cache()
+    res["verify-b64-q4"] = run_verify_extra(pkv, dev, hbm_peak, flush, stream)
     return res
+
+
+def run_verify_extra(pkv, dev, hbm_peak, flush, stream):
+    """Speculative verify: the decode-b64 batch with 4 proposed tokens per
+    sequence (q_len = 4), through the multi-query decode and, for comparison,
+    through the 128-row tcgen05 prefill on the same inputs.  L2 flushed before
+    each timed call."""
+    qn = 4
+    lens = W._uniform_ints(512, 4096, 64, W.seed_for(2))
+    w = W.make_prefill([L - qn for L in lens], [qn] * len(lens), 16, 8, 2048,
+                       W.seed_for(2) + 1, name="verify-b64-q4", pool_device=dev)
+    q = w.q.to(dev)
+    kc, vc = w.k_cache, w.v_cache
+    tables, cq, ck = w.block_tables.to(dev), w.cu_seqlens_q.to(dev), w.cu_seqlens_k.to(dev)
+    ctx = torch.tensor(w.k_lens, dtype=torch.int32, device=dev)
+    q4 = q.view(w.B, qn, w.Hq, w.D)
+    out, lse = torch.empty_like(q4), torch.empty((w.B, qn, w.Hq), dtype=torch.float32, device=dev)
+    need = pkv.paged_decode_multiquery_workspace_bytes(w.B, qn, w.Hq, w.Hkv, w.D, tables.shape[1])
+    ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        for _ in range(5):
+            fn()
+        times = []
+        for _ in range(30):
+            _flush_l2(flush)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            times.append((a, b))
+        torch.cuda.synchronize()
+        ms = sorted(x.elapsed_time(y) for x, y in times)
+        return ms[len(ms) // 2]
+
+    med = timed(lambda: pkv.paged_decode_attention_multiquery(
+        q4, kc, vc, tables, ctx, w.scale, out=out, lse=lse, workspace=ws, stream=stream))
+    kv_tokens = int(sum(w.k_lens))
+    nbytes = kv_tokens * w.Hkv * w.D * 2 * 2 + 2 * q.numel() * 2 + lse.numel() * 4
+    out2 = torch.empty_like(q)
+    lse2 = torch.empty((q.shape[0], w.Hq), dtype=torch.float32, device=dev)
+    med_p = timed(lambda: pkv.paged_prefill_attention(
+        q, kc, vc, tables, cq, ck, w.max_seqlen_q, w.max_seqlen_k, w.scale, out=out2, lse=lse2,
+        stream=stream))
+    gbs = nbytes / (med / 1e3) / 1e9
+    return {"workload": w.name, "q_len": qn, "median_us": round(med * 1e3, 2),
+            "kv_tokens": kv_tokens, "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / hbm_peak, 4),
+            "verified_tokens_per_s": round(w.B * qn / (med / 1e3), 1),
+            "prefill_path_us": round(med_p * 1e3, 2),
+            "note": "paged_decode_attention_multiquery (tensor-core kernel, one (sequence, kv "
+                    "head) tile of g*q_len rows, K/V read once per kv head); prefill_path_us: "
+                    "the same batch through paged_prefill_attention (one tile per query head)"}
 
 
 def _traffic(workload: str, algorithmic: int):

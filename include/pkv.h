@@ -234,9 +234,12 @@ int paged_decode_attention_noalloc(void* out, float* lse, const void* q,
  * speculative decoding, which turns sequential decode into a parallel
  * "mini-prefill" ("What Is an Inference Engine, Anyway?", Technical details,
  * Speculative Decoding).  Same operation as paged_prefill_attention with
- * Lq = q_len and Lk = context_lens[b] for every sequence, computed by the
- * split-K decode kernel (memory bound, like decode) instead of 128-row tensor
- * core tiles.
+ * Lq = q_len and Lk = context_lens[b] for every sequence.  With
+ * num_splits = 0, g*q_len <= 128 (g = Hq/Hkv) and at least one (sequence, kv
+ * head) pair per SM, it runs on the tensor cores with all g*q_len (position,
+ * head) rows of a kv head in one tile, so each kv head's K/V are read once and
+ * no workspace is used (the size query returns 0); otherwise on the split-K
+ * decode kernel over g*q_len rows per kv head.
  * q   : bf16 [B, q_len, Hq, D] contiguous.   out : bf16 [B, q_len, Hq, D].
  * lse : f32 [B, q_len, Hq] (natural log) or NULL.
  * context_lens[b] counts every cached token of sequence b, its q_len new ones

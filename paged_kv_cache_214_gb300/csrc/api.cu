@@ -191,11 +191,21 @@ extern "C" int paged_decode_attention(void* out, float* lse, const void* q, cons
 // Longest run of query positions per sequence the multi-query decode accepts.
 constexpr int kMaxQueryLen = 64;
 
+// Multi-query decode on the tensor-core kernel (one item per (sequence, kv
+// head), all g*q_len rows in one tile) when the rows fit one tile and there
+// are at least as many items as SMs; otherwise (small batches, or a split
+// count the caller asks for) on the split-K decode kernel.
+bool use_verify_kernel(int B, int q_len, int Hq, int Hkv, int num_splits) {
+  if (num_splits != 0 || q_len < 2 || !verify_rows_fit(Hq / Hkv, q_len)) return false;
+  return static_cast<int64_t>(B) * Hkv >= device_sm_count();
+}
+
 extern "C" size_t paged_decode_multiquery_workspace_bytes(int B, int q_len, int Hq, int Hkv,
                                                           int D, int max_blocks_per_seq,
                                                           int block_size, int num_splits) {
   if (D != kHeadDim || block_size != kBlockSize || num_splits < 0) return 0;
   if (q_len < 1 || q_len > kMaxQueryLen) return 0;
+  if (Hkv > 0 && Hq % Hkv == 0 && use_verify_kernel(B, q_len, Hq, Hkv, num_splits)) return 0;
   DecodePlan plan;
   if (plan_decode(B, Hq * q_len, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), 0,
                   &plan))
@@ -219,6 +229,13 @@ extern "C" int paged_decode_attention_multiquery(
   if (num_blocks == 0 && max_blocks_per_seq > 0) return PKV_ERR_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PKV_ERR_ARG;
+  if (use_verify_kernel(B, q_len, Hq, Hkv, num_splits)) {
+    unsigned* err = device_error_word();
+    if (!err) return PKV_ERR_LAUNCH;
+    VerifyArgs va{out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                  context_lens, B, q_len, Hq, Hkv, num_blocks, scale};
+    return launch_verify(va, err, reinterpret_cast<cudaStream_t>(stream));
+  }
   DecodePlan plan;
   st = plan_decode(B, Hq * q_len, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), 0,
                    &plan);

@@ -143,7 +143,9 @@ __device__ __forceinline__ float rescale(float m, float mn) {
   return m == -INFINITY ? 0.f : ex2(m - mn);
 }
 
-template <int G, int KVH>
+// kMQ: several query positions per sequence (q_len > 1); plain decode
+// compiles without the per-row key limits.
+template <int G, int KVH, bool kMQ>
 __global__ void __launch_bounds__(kThreads, 2)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
@@ -192,18 +194,17 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     ctx = ctx < P ? P : cap;
   }
   // several query positions: every one of the q_len new tokens is in the cache
-  if (p.q_len > 1 && ctx < p.q_len && tid == 0 && split == 0 && hg == 0)
-    record_error(p.err, kErrIndex);
+  if (kMQ && ctx < p.q_len && tid == 0 && split == 0 && hg == 0) record_error(p.err, kErrIndex);
   // row of q / out / lse for virtual head v, and the number of keys it sees
   // (position i of q_len sees keys j < ctx - q_len + 1 + i)
   const int gp = g / p.q_len;
   auto phys_row = [&](int v) -> int64_t {
-    if (p.q_len == 1) return static_cast<int64_t>(b) * p.Hq + v;
+    if (!kMQ) return static_cast<int64_t>(b) * p.Hq + v;
     const int kv = v / g, r = v - kv * g;
     return (static_cast<int64_t>(b) * p.q_len + r / gp) * p.Hq_phys + kv * gp + r % gp;
   };
   auto key_limit = [&](int v) -> int {
-    if (p.q_len == 1) return ctx;
+    if (!kMQ) return ctx;
     return ctx - (p.q_len - 1 - (v % g) / gp);
   };
   const int nsplit = (ctx - P + split_tokens - 1) / split_tokens;
@@ -313,7 +314,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     for (int h = 0; h < G; ++h) {
       m[h] = -INFINITY;
       l[h] = 0.f;
-      lim[h] = key_limit(qhead(my_hh, h)) - tok_begin;
+      lim[h] = kMQ ? key_limit(qhead(my_hh, h)) - tok_begin : 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) o2[h][i] = 0ull;
     }
@@ -357,7 +358,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
           acc += __shfl_xor_sync(0xffffffffu, acc, 1);
           acc += __shfl_xor_sync(0xffffffffu, acc, 2);
           acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-          sc[r][h] = (t < n_valid && it * kTT + t < lim[h]) ? acc : -INFINITY;
+          sc[r][h] = (t < n_valid && (!kMQ || it * kTT + t < lim[h])) ? acc : -INFINITY;
         }
       }
       // online softmax, once per tile.  The running max only moves when the
@@ -377,7 +378,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const int t = 4 * (r * kWPH + my_wl) + grp;
-          sc[r][h] = (t < n_valid && it * kTT + t < lim[h]) ? ex2(sc[r][h] - m[h]) : 0.f;
+          sc[r][h] = (t < n_valid && (!kMQ || it * kTT + t < lim[h])) ? ex2(sc[r][h] - m[h]) : 0.f;
           l[h] += sc[r][h];
         }
       }
@@ -530,7 +531,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   if (tid == 0) *counter = 0u;  // ready for the next call
 }
 
-template <int G, int KVH>
+template <int G, int KVH, bool kMQ>
 int launch_g(const DecodeArgs& a, const DecodePlan& plan, const DecodeParams& prm,
              const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t stream) {
   using L = SmemLayout<G>;
@@ -539,13 +540,14 @@ int launch_g(const DecodeArgs& a, const DecodePlan& plan, const DecodeParams& pr
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(paged_decode_kernel<G, KVH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(paged_decode_kernel<G, KVH, kMQ>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::kBytes) != cudaSuccess)
       return PKV_ERR_LAUNCH;
     attr_set[dev] = true;
   }
   dim3 grid(plan.num_splits, (a.Hkv / KVH) * plan.head_groups, a.B);
-  paged_decode_kernel<G, KVH><<<grid, kThreads, L::kBytes, stream>>>(km, vm, prm);
+  paged_decode_kernel<G, KVH, kMQ><<<grid, kThreads, L::kBytes, stream>>>(km, vm, prm);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }
 
@@ -677,9 +679,15 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
     prm.ws_count = nullptr;
   }
   switch (plan.heads_per_cta) {
-    case 4: return launch_g<4, 1>(a, plan, prm, km, vm, stream);
-    case 2: return launch_g<2, 1>(a, plan, prm, km, vm, stream);
-    default: return launch_g<1, 1>(a, plan, prm, km, vm, stream);
+    case 4:
+      return a.q_len > 1 ? launch_g<4, 1, true>(a, plan, prm, km, vm, stream)
+                         : launch_g<4, 1, false>(a, plan, prm, km, vm, stream);
+    case 2:
+      return a.q_len > 1 ? launch_g<2, 1, true>(a, plan, prm, km, vm, stream)
+                         : launch_g<2, 1, false>(a, plan, prm, km, vm, stream);
+    default:
+      return a.q_len > 1 ? launch_g<1, 1, true>(a, plan, prm, km, vm, stream)
+                         : launch_g<1, 1, false>(a, plan, prm, km, vm, stream);
   }
 }
 

@@ -122,4 +122,24 @@ struct PrefillArgs {
 };
 int launch_prefill(const PrefillArgs& a, unsigned* err, cudaStream_t stream);
 
+// q_len new positions per sequence (speculative verify) on the tensor-core
+// kernel: one item per (sequence, kv head) holding its g*q_len (position, head)
+// rows; needs g*q_len <= 128 (verify_rows_fit).  q [B, q_len, Hq, 128],
+// out like q, lse [B, q_len, Hq] natural log or null.
+struct VerifyArgs {
+  void* out;
+  float* lse;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  int max_blocks_per_seq;
+  const int32_t* context_lens;
+  int B, q_len, Hq, Hkv;
+  int64_t num_blocks;
+  float scale;
+};
+int verify_rows_fit(int g, int q_len);
+int launch_verify(const VerifyArgs& a, unsigned* err, cudaStream_t stream);
+
 }  // namespace pkv

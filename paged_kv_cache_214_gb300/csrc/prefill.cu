@@ -9,7 +9,8 @@
 // table and the "concatenation" is simply the table.  Query row r of a chunk of
 // Lq rows over Lk keys sees keys j <= Lk - Lq + r.  Prefill is the compute-heavy
 // phase (same page, "Differences", §3), so both products run on tensor cores.
-// The same kernel computes the shared-prefix pass of a decode batch (kPrefix).
+// The same kernel computes the shared-prefix pass of a decode batch and the
+// verify step of speculative decoding (see the modes below).
 //
 // Work item: one 128-row query tile (one sequence and query head) and its key
 // tiles.  The kernel is persistent: one block per SM walks the items, heaviest
@@ -95,6 +96,14 @@ constexpr float kLazyRescale = 8.f;    // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr uint32_t kFull = 0xffffffffu;
 
+// Kernel modes.  kCausal: (chunked) prefill, one item per (row tile, sequence,
+// query head).  kPrefixPass: the shared-prefix pass of a decode batch.
+// kVerify: q_len new positions per sequence (speculative verify), one item per
+// (sequence, kv head) whose tile holds the g*q_len (position, head) rows.
+constexpr int kCausal = 0;
+constexpr int kPrefixPass = 1;
+constexpr int kVerify = 2;
+
 struct PrefillParams {
   __nv_bfloat16* out;
   float* lse;
@@ -105,6 +114,8 @@ struct PrefillParams {
   int splits;        // shared-prefix mode: key ranges
   int rows_per_tile; // shared-prefix mode: (sequence, head) rows per query tile
   int n_rt;          // shared-prefix mode: query tiles per kv head
+  int q_len;         // verify mode: query positions per sequence
+  const int32_t* ctx;  // verify mode: keys per sequence
   const __nv_bfloat16* q;
   const int32_t* block_tables;
   const int32_t* cu_q;
@@ -132,7 +143,7 @@ struct Item {
   const int32_t* table;
 };
 
-template <bool kPrefix>
+template <int kMode>
 __device__ __forceinline__ Item get_item(const PrefillParams& p, int idx, bool report) {
   Item it;
   const int g = p.Hq / p.Hkv;
@@ -140,7 +151,28 @@ __device__ __forceinline__ Item get_item(const PrefillParams& p, int idx, bool r
   it.h = 0;
   it.q_begin = 0;
   it.z = 0;
-  if constexpr (kPrefix) {
+  if constexpr (kMode == kVerify) {
+    // rows r = position r/g, head kvh*g + r%g of sequence b; row r sees keys
+    // j <= Lk - q_len + r/g
+    const int b = idx / p.Hkv;
+    it.kvh = idx - b * p.Hkv;
+    it.h = it.kvh * g;
+    it.q_begin = b * p.q_len;
+    it.q0 = 0;
+    it.kt0 = 0;
+    it.z = 0;
+    it.table = p.block_tables + static_cast<int64_t>(b) * p.maxblk;
+    const int Lk = p.ctx[b];
+    it.Lk = Lk;
+    it.rows = g * p.q_len;
+    it.diag = Lk - p.q_len;
+    if (Lk < p.q_len || static_cast<int64_t>(Lk) > static_cast<int64_t>(p.maxblk) * kBlockSize) {
+      if (report) record_error(p.err, kErrIndex);
+      it.rows = 0;
+      return it;
+    }
+    it.n = (Lk + kN - 1) / kN;
+  } else if constexpr (kMode == kPrefixPass) {
     const int grp = idx / p.n_rt;
     const int rt = idx - grp * p.n_rt;
     it.kvh = grp / p.splits;
@@ -190,13 +222,13 @@ __device__ __forceinline__ int item_index(int k) {
 }
 
 // First non-empty item at or after round k (k is advanced to it).
-template <bool kPrefix>
+template <int kMode>
 __device__ __forceinline__ bool next_item(const PrefillParams& p, int n_rounds, int& k, Item& it,
                                           bool report) {
   for (; k < n_rounds; ++k) {
     const int idx = item_index(k);
     if (idx >= p.n_items) continue;
-    it = get_item<kPrefix>(p, idx, report);
+    it = get_item<kMode>(p, idx, report);
     if (it.n > 0) return true;
   }
   return false;
@@ -241,14 +273,18 @@ struct BlockIds {
   }
 };
 
-// kPrefix = false: causal (chunked) prefill over (row tile, sequence, query head) items.
-// kPrefix = true: the shared-prefix pass of a decode batch.  For kv head kvh the
+// kCausal: causal (chunked) prefill over (row tile, sequence, query head) items.
+// kPrefixPass: the shared-prefix pass of a decode batch.  For kv head kvh the
 // query rows are the B*g (sequence, query head) pairs of its group (row r =
 // sequence r/g, head kvh*g + r%g); every row sees all prefix_tokens keys of the
 // blocks that open table row 0, split into key ranges; the output is a
 // normalised fp32 partial and its log2-sum-exp per range, merged into the
 // decode result afterwards.
-template <bool kPrefix>
+// kVerify: for sequence b and kv head kvh the rows are the g*q_len (position,
+// head) pairs (row r = position r/g, head kvh*g + r%g), read by one TMA box
+// of g heads x q_len tokens; row r sees the keys a decode of position r/g
+// would see.
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                      const __grid_constant__ CUtensorMap kmap,
@@ -267,6 +303,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
   const int lane = tid & 31;
   const int g = p.Hq / p.Hkv;
   const int n_rounds = (p.n_items + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+  constexpr bool kPrefix = kMode == kPrefixPass;
   const int table_limit = kPrefix ? p.prefix_tokens / kBlockSize : p.maxblk;
 
   if (tid == 0) {
@@ -306,7 +343,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
     auto load_q = [&](const Item& it, int qi) -> bool {
       const uint32_t qdst = sbase + kOffQ;
       if (qi >= 1 && !warp_wait(bar(kBarQEmpty), (qi - 1) & 1)) return false;
-      if (!kPrefix && it.rows < kM) {
+      if (kMode == kCausal && it.rows < kM) {
         // ragged last tile of a sequence: gather its rows (zero-fill the rest)
         const __nv_bfloat16* base =
             p.q + (static_cast<int64_t>(it.q_begin + it.q0) * p.Hq + it.h) * kHeadDim;
@@ -324,13 +361,16 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
         if (lane == 0) mbar_arrive(bar(kBarQFull));
       } else {
         if (lane == 0)
-          mbar_arrive_expect_tx(bar(kBarQFull), kPrefix ? p.rows_per_tile * 256 : kTile);
+          mbar_arrive_expect_tx(bar(kBarQFull), kMode == kCausal ? kTile : p.rows_per_tile * 256);
         __syncwarp();
         if (lane >= 2 * kKStages && lane < 2 * kKStages + 2) {   // lanes of their own
           const int hf = lane & 1;
           if constexpr (kPrefix) {
             // (sequence, head) rows of the group: box {64 dims, g heads, tokens}
             tma_load_3d(qdst + hf * kHalf, &qmap, bar(kBarQFull), hf * 64, it.kvh * g, it.q0 / g);
+          } else if constexpr (kMode == kVerify) {
+            // (position, head) rows: box {64 dims, g heads, q_len tokens}
+            tma_load_3d(qdst + hf * kHalf, &qmap, bar(kBarQFull), hf * 64, it.h, it.q_begin);
           } else {
             tma_load_3d(qdst + hf * kHalf, &qmap, bar(kBarQFull), hf * 64, it.h,
                         it.q_begin + it.q0);
@@ -343,11 +383,11 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
     };
     int k = 0;
     Item it;
-    bool have = next_item<kPrefix>(p, n_rounds, k, it, false);
+    bool have = next_item<kMode>(p, n_rounds, k, it, false);
     while (have && ok) {
       int k2 = k + 1;
       Item nx;
-      const bool have_next = next_item<kPrefix>(p, n_rounds, k2, nx, false);
+      const bool have_next = next_item<kMode>(p, n_rounds, k2, nx, false);
       ids.chunk = -1;
       for (int kt = 0; kt < it.n; ++kt, ++gk, rk.next()) {
         if (__any_sync(kFull, flags[0] != 0)) { ok = false; break; }
@@ -391,11 +431,11 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
     Ring<kVStages> rv;
     int k = 0;
     Item it;
-    bool have = next_item<kPrefix>(p, n_rounds, k, it, false);
+    bool have = next_item<kMode>(p, n_rounds, k, it, false);
     while (have && ok) {
       int k2 = k + 1;
       Item nx;
-      const bool have_next = next_item<kPrefix>(p, n_rounds, k2, nx, false);
+      const bool have_next = next_item<kMode>(p, n_rounds, k2, nx, false);
       ids.chunk = -1;
       for (int kt = 0; kt < it.n; ++kt, ++gk, rv.next()) {
         if (__any_sync(kFull, flags[0] != 0)) { ok = false; break; }
@@ -432,11 +472,11 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
       Ring<kKStages> rk;
       int k = 0;
       Item it;
-      bool have = next_item<kPrefix>(p, n_rounds, k, it, false);
+      bool have = next_item<kMode>(p, n_rounds, k, it, false);
       while (have && ok) {
         int k2 = k + 1;
         Item nx;
-        const bool have_next = next_item<kPrefix>(p, n_rounds, k2, nx, false);
+        const bool have_next = next_item<kMode>(p, n_rounds, k2, nx, false);
         if (!mbar_wait(bar(kBarQFull), gi & 1)) { ok = false; timeout = true; break; }
         const uint32_t q_s = sbase + kOffQ;
         for (int kt = 0; kt < it.n; ++kt, ++gk, sb.next(), rk.next()) {
@@ -484,11 +524,11 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
       const uint32_t d_o = tmem + kColO;
       int k = 0;
       Item it;
-      bool have = next_item<kPrefix>(p, n_rounds, k, it, false);
+      bool have = next_item<kMode>(p, n_rounds, k, it, false);
       while (have && ok) {
         int k2 = k + 1;
         Item nx;
-        const bool have_next = next_item<kPrefix>(p, n_rounds, k2, nx, false);
+        const bool have_next = next_item<kMode>(p, n_rounds, k2, nx, false);
         for (int kt = 0; kt < it.n; ++kt, ++gk, sb.next(), rv.next()) {
           if (flags[0]) { ok = false; break; }
           if (!mbar_wait(bar(kBarVFull + rv.idx), rv.ph) ||
@@ -564,6 +604,10 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
         const int ga = e.q0 + ra, gb = e.q0 + rb;
         rowa = (static_cast<int64_t>(ga / g) * p.Hq + e.kvh * g + ga % g) * p.splits + e.z;
         rowb = (static_cast<int64_t>(gb / g) * p.Hq + e.kvh * g + gb % g) * p.splits + e.z;
+      } else if constexpr (kMode == kVerify) {
+        // row r: position r/g of the sequence, head kvh*g + r%g
+        rowa = static_cast<int64_t>(e.q_begin + ra / g) * p.Hq + e.h + ra % g;
+        rowb = static_cast<int64_t>(e.q_begin + rb / g) * p.Hq + e.h + rb % g;
       } else {
         rowa = static_cast<int64_t>(e.q_begin + e.q0 + ra) * p.Hq + e.h;
         rowb = static_cast<int64_t>(e.q_begin + e.q0 + rb) * p.Hq + e.h;
@@ -603,12 +647,14 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
     f32x2 pla = 0ull, plb = 0ull;
     int k = 0;
     Item it;
-    bool have = next_item<kPrefix>(p, n_rounds, k, it, warp == 0 && lane == 0);
+    bool have = next_item<kMode>(p, n_rounds, k, it, warp == 0 && lane == 0);
     while (have && ok) {
       int k2 = k + 1;
       Item nx;
-      const bool have_next = next_item<kPrefix>(p, n_rounds, k2, nx, warp == 0 && lane == 0);
-      const int visa = it.diag + ra, visb = it.diag + rb;   // last visible keys
+      const bool have_next = next_item<kMode>(p, n_rounds, k2, nx, warp == 0 && lane == 0);
+      // last visible keys: row r is query position r (r / g in verify mode)
+      const int visa = it.diag + (kMode == kVerify ? ra / g : ra);
+      const int visb = it.diag + (kMode == kVerify ? rb / g : rb);
       float ma = -INFINITY, mb = -INFINITY;
       f32x2 la2 = pack2(0.f, 0.f), lb2 = pack2(0.f, 0.f);  // running sums, as pairs
       for (int kt = 0; kt < it.n; ++kt, ++gk, sb.next(), rv.next()) {
@@ -760,13 +806,13 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
   }
 }
 
-template <bool kPrefix>
+template <int kMode>
 bool set_smem_attr() {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(paged_prefill_kernel<kPrefix>,
+    if (cudaFuncSetAttribute(paged_prefill_kernel<kMode>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes) != cudaSuccess)
       return false;
@@ -818,8 +864,8 @@ int launch_prefill(const PrefillArgs& a, unsigned* err, cudaStream_t stream) {
   prm.n_items = static_cast<int>(items);
   prm.num_blocks = a.num_blocks;
   prm.scale_log2 = a.scale * 1.4426950408889634f;
-  if (!set_smem_attr<false>()) return PKV_ERR_LAUNCH;
-  paged_prefill_kernel<false><<<grid_for(prm.n_items), kThreads, kSmemBytes, stream>>>(
+  if (!set_smem_attr<kCausal>()) return PKV_ERR_LAUNCH;
+  paged_prefill_kernel<kCausal><<<grid_for(prm.n_items), kThreads, kSmemBytes, stream>>>(
       qm, km, vm, prm);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }
@@ -855,8 +901,47 @@ int launch_prefix_attention(const PrefixArgs& a, unsigned* err, cudaStream_t str
   const int64_t items = static_cast<int64_t>(prm.n_rt) * a.Hkv * a.splits;
   if (items > INT32_MAX) return PKV_ERR_SHAPE;
   prm.n_items = static_cast<int>(items);
-  if (!set_smem_attr<true>()) return PKV_ERR_LAUNCH;
-  paged_prefill_kernel<true><<<grid_for(prm.n_items), kThreads, kSmemBytes, stream>>>(
+  if (!set_smem_attr<kPrefixPass>()) return PKV_ERR_LAUNCH;
+  paged_prefill_kernel<kPrefixPass><<<grid_for(prm.n_items), kThreads, kSmemBytes, stream>>>(
+      qm, km, vm, prm);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+}
+
+int verify_rows_fit(int g, int q_len) { return g >= 1 && q_len >= 1 && g * q_len <= kM; }
+
+int launch_verify(const VerifyArgs& a, unsigned* err, cudaStream_t stream) {
+  if (a.B == 0) return PKV_OK;
+  const int g = a.Hq / a.Hkv;
+  if (!verify_rows_fit(g, a.q_len)) return PKV_ERR_SHAPE;
+  const int64_t q_rows = static_cast<int64_t>(a.B) * a.q_len;
+  if (q_rows > INT32_MAX) return PKV_ERR_SHAPE;
+  CUtensorMap qm, km, vm;
+  const int64_t slots = a.num_blocks * kBlockSize;
+  // q [B*q_len, Hq, 128]: a box is 64 dims x the g heads of one kv head x q_len positions
+  if (!encode_pool_map(&qm, a.q, q_rows, a.Hq, a.q_len, g) ||
+      !encode_pool_map(&km, a.k_cache, slots, a.Hkv, kN) ||
+      !encode_pool_map(&vm, a.v_cache, slots, a.Hkv, kN))
+    return PKV_ERR_ARG;
+  PrefillParams prm = {};
+  prm.out = static_cast<__nv_bfloat16*>(a.out);
+  prm.lse = a.lse;
+  prm.q = static_cast<const __nv_bfloat16*>(a.q);
+  prm.block_tables = a.block_tables;
+  prm.ctx = a.context_lens;
+  prm.err = err;
+  prm.B = a.B;
+  prm.Hq = a.Hq;
+  prm.Hkv = a.Hkv;
+  prm.maxblk = a.max_blocks_per_seq;
+  prm.q_len = a.q_len;
+  prm.rows_per_tile = g * a.q_len;
+  prm.num_blocks = a.num_blocks;
+  prm.scale_log2 = a.scale * 1.4426950408889634f;
+  const int64_t items = static_cast<int64_t>(a.B) * a.Hkv;
+  if (items > INT32_MAX) return PKV_ERR_SHAPE;
+  prm.n_items = static_cast<int>(items);
+  if (!set_smem_attr<kVerify>()) return PKV_ERR_LAUNCH;
+  paged_prefill_kernel<kVerify><<<grid_for(prm.n_items), kThreads, kSmemBytes, stream>>>(
       qm, km, vm, prm);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }

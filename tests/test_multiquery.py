@@ -44,14 +44,42 @@ def run_and_check(w, q_len, num_splits=0, what=""):
     return assert_close(out.view(-1, w.Hq, w.D), lse.view(-1, w.Hq), ref_o, ref_l, what)
 
 
+def tensor_core_path(w, q_len):
+    """True when the call runs on the tensor-core verify kernel (which needs
+    no workspace) rather than the split-K decode kernel."""
+    return pkv.paged_decode_multiquery_workspace_bytes(
+        w.B, q_len, w.Hq, w.Hkv, w.D, w.block_tables.shape[1]) == 0
+
+
+# 24 ragged sequences (across block and tile boundaries, some holding nothing
+# but the new tokens): 24 x 8 kv heads = 192 items, the tensor-core path
+CACHED_24 = [0, 1, 63, 64, 127, 128, 255, 256, 300, 511, 512, 700,
+             999, 1024, 1100, 1500, 1777, 2000, 2047, 2048, 2300, 2600, 3000, 3500]
+
+
 @pytest.mark.parametrize("q_len", [2, 4, 8])
 @pytest.mark.parametrize("Hq,Hkv", [(16, 8), (32, 8), (8, 8), (24, 8)])
-def test_verify_shapes(q_len, Hq, Hkv):
-    # ragged contexts across block and tile boundaries; some sequences are
-    # nothing but the new tokens
+def test_verify_tensor_core_path(q_len, Hq, Hkv):
+    w = verify_batch(CACHED_24, q_len, Hq, Hkv, 512, 7000 + 10 * q_len + Hq)
+    assert tensor_core_path(w, q_len)
+    run_and_check(w, q_len, what=f"tcgen05 q_len={q_len} Hq={Hq} Hkv={Hkv}")
+
+
+@pytest.mark.parametrize("q_len", [2, 4, 8])
+@pytest.mark.parametrize("Hq,Hkv", [(16, 8), (32, 8), (8, 8), (24, 8)])
+def test_verify_split_decode_path(q_len, Hq, Hkv):
+    # 9 sequences x 8 kv heads: too few items for the tensor-core path
     cached = [0, 1, 63, 64, 255, 256, 700, 1500, 2047]
-    w = verify_batch(cached, q_len, Hq, Hkv, 96, 7000 + 10 * q_len + Hq)
-    run_and_check(w, q_len, what=f"q_len={q_len} Hq={Hq} Hkv={Hkv}")
+    w = verify_batch(cached, q_len, Hq, Hkv, 96, 7050 + 10 * q_len + Hq)
+    assert not tensor_core_path(w, q_len)
+    run_and_check(w, q_len, what=f"split decode q_len={q_len} Hq={Hq} Hkv={Hkv}")
+
+
+def test_rows_beyond_one_tile_use_split_decode():
+    # g * q_len = 16 * 16 = 256 rows per kv head: more than one 128-row tile
+    w = verify_batch(CACHED_24[:12], 16, 32, 2, 256, 7060)
+    assert not tensor_core_path(w, 16)
+    run_and_check(w, 16, what="g*q_len > 128")
 
 
 @pytest.mark.parametrize("num_splits", [1, 2, 5, 16])
@@ -97,4 +125,5 @@ def test_verify_batch_of_decode_size():
     # batch-64 verify of 4 proposed tokens over contexts like the decode bench
     lens = W._uniform_ints(512, 4096, 64, W.seed_for(2))
     w = verify_batch([L - 4 for L in lens], 4, 16, 8, 1200, 7400)
+    assert tensor_core_path(w, 4)
     run_and_check(w, 4, what="b64 verify")
