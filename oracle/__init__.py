@@ -18,6 +18,10 @@ Every function cites the passage of the source pages it follows:
   tokens) and §2 "Scheduler" (chunked prefill), bottom-right causal mask;
 * the attention formula softmax(q k^T) v — "Why Understand Inference Engine
   Architecture?", TorchScript Optimization; scale 1/sqrt(D) is an argument.
+* e4m3_table / quantize_e4m3 / store_fp8 / decode_fp8 — an FP8 (OCP E4M3)
+  KV cache with one scale per tensor; the pages only name quantized KV
+  transfers ("Why Understand Inference Engine Architecture?", Tensor
+  Parallelism Optimization), so the format is this build's reading.
 
 bf16 tensors are passed as uint16 bit patterns; outputs are float64.
 """
@@ -74,8 +78,15 @@ def _declare(lib):
     lib.oracle_prefill.argtypes = [P, P, P, P, P, P, i32, P, P, i32, i32, i32,
                                    i32, i32, i64, f64, i32]
     lib.oracle_copy_blocks.argtypes = [P, P, P, P, i64, i32, i32, i32, i64]
+    f32 = ctypes.c_float
+    lib.oracle_e4m3_table.argtypes = [P]
+    lib.oracle_quantize_e4m3.argtypes = [P, i64, f32, P]
+    lib.oracle_store_fp8.argtypes = [P, P, i64, i64, P, P, P, i64, i32, i32, i32, i64, f32, f32]
+    lib.oracle_decode_fp8.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i64,
+                                      f64, f64, f64, i32]
     for fn in ("oracle_store", "oracle_gather", "oracle_decode", "oracle_prefill",
-               "oracle_hardware_threads", "oracle_copy_blocks"):
+               "oracle_hardware_threads", "oracle_copy_blocks", "oracle_e4m3_table",
+               "oracle_quantize_e4m3", "oracle_store_fp8", "oracle_decode_fp8"):
         getattr(lib, fn).restype = ctypes.c_int
     return lib
 
@@ -190,4 +201,63 @@ def prefill(q, k_cache, v_cache, block_tables, cu_seqlens_q, cu_seqlens_k, scale
     _check(lib.oracle_prefill(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache),
                               _ptr(v_cache), _ptr(bt), maxblk, _ptr(cq), _ptr(ck), B,
                               Hq, Hkv, D, bs, NB, float(scale), int(nthreads)))
+    return out, lse
+
+
+def inv_scale(scale: float) -> np.float32:
+    """The binary32 reciprocal of a tensor scale, as the quantizer uses it."""
+    return np.float32(1.0) / np.float32(scale)
+
+
+def e4m3_table(lib=None) -> np.ndarray:
+    """Value of each of the 256 E4M3 codes (float64, NaN for 0x7F / 0xFF)."""
+    lib = lib or load()
+    t = np.empty(256, np.float64)
+    _check(lib.oracle_e4m3_table(_ptr(t)))
+    return t
+
+
+def quantize_e4m3(x_bits, scale: float, lib=None) -> np.ndarray:
+    """E4M3 codes (uint8, same shape) of bf16 values x under tensor scale."""
+    lib = lib or load()
+    x = _u16(x_bits)
+    codes = np.empty(x.shape, np.uint8)
+    _check(lib.oracle_quantize_e4m3(_ptr(x), x.size, float(inv_scale(scale)), _ptr(codes)))
+    return codes
+
+
+def store_fp8(k, v, k_cache, v_cache, slot_mapping, k_scale: float, v_scale: float,
+              lib=None) -> None:
+    """In-place store of bf16 k/v [T, Hkv, D] into uint8 E4M3 caches [NB, bs, Hkv, D]."""
+    lib = lib or load()
+    k, v = _u16(k), _u16(v)
+    for c in (k_cache, v_cache):
+        if c.dtype != np.uint8 or not c.flags.c_contiguous:
+            raise TypeError("fp8 caches must be C-contiguous uint8")
+    T, Hkv, D = k.shape
+    NB, bs = k_cache.shape[0], k_cache.shape[1]
+    sm = _i32(slot_mapping)
+    _check(lib.oracle_store_fp8(_ptr(k), _ptr(v), Hkv * D, Hkv * D, _ptr(k_cache),
+                                _ptr(v_cache), _ptr(sm), T, Hkv, D, bs, NB,
+                                float(inv_scale(k_scale)), float(inv_scale(v_scale))))
+
+
+def decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale,
+               nthreads=0, lib=None):
+    """Decode over uint8 E4M3 caches: out [B, Hq, D] float64, lse [B, Hq] float64."""
+    lib = lib or load()
+    q = _u16(q)
+    for c in (k_cache, v_cache):
+        if c.dtype != np.uint8 or not c.flags.c_contiguous:
+            raise TypeError("fp8 caches must be C-contiguous uint8")
+    B, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    assert D == D2
+    bt, cl = _i32(block_tables), _i32(context_lens)
+    maxblk = bt.shape[1] if bt.ndim == 2 else 0
+    out = np.zeros((B, Hq, D), np.float64)
+    lse = np.zeros((B, Hq), np.float64)
+    _check(lib.oracle_decode_fp8(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                 _ptr(bt), maxblk, _ptr(cl), B, Hq, Hkv, D, bs, NB, float(scale),
+                                 float(k_scale), float(v_scale), int(nthreads)))
     return out, lse

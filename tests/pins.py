@@ -16,6 +16,11 @@ What pins what:
 * invariances — physical block relabelling and prefix sharing (bit-identical),
   causal perturbation, chunked vs whole prefill, prefill with one query row vs
   decode, GQA vs MHA with repeated K/V.
+* FP8 (E4M3) cache — the code table against torch's float8_e4m3fn and fixed
+  anchors of the format; the quantizer against a brute-force search for the
+  nearest finite code (ties to the even code) and against torch's conversion
+  in range; the FP8 store's addressing; the FP8 decode against the bf16 decode
+  on a pool holding the same values.
 """
 
 from __future__ import annotations
@@ -429,6 +434,123 @@ def pin_prefill_rejects_lk_lt_lq(lib):
     raise AssertionError("Lk < Lq was accepted")
 
 
+# ---------------------------------------------------------------- FP8 (E4M3)
+
+def _finite_codes(table):
+    codes = np.array([c for c in range(256) if np.isfinite(table[c])], np.int64)
+    return codes, table[codes]
+
+
+def _nearest_code(v: float, codes, vals) -> int:
+    """Brute force: the finite code nearest to v, ties to the even code; the
+    search runs over magnitudes (codes 0x00..0x7E) and the sign of v is put back
+    on the result (so -0 and tiny negatives give 0x80).  Past the largest finite
+    magnitude the nearest finite value is that magnitude itself."""
+    if math.isnan(v):
+        return 0x7F
+    a = abs(v)
+    pos = codes < 0x80
+    pc, pv = codes[pos], vals[pos]
+    if a >= pv.max():
+        c = int(pc[np.argmax(pv)])
+    else:
+        d = np.abs(pv - a)
+        cand = pc[d == d.min()]
+        c = int(cand[0]) if len(cand) == 1 else int([x for x in cand if x % 2 == 0][0])
+    return c | 0x80 if math.copysign(1.0, v) < 0 else c
+
+
+def pin_e4m3_table(lib):
+    t = O.e4m3_table(lib=lib)
+    # fixed anchors of the format: sign, bias 7, 3 mantissa bits, subnormals
+    assert t[0x00] == 0.0 and t[0x01] == 2.0 ** -9 and t[0x07] == 7 * 2.0 ** -9
+    assert t[0x08] == 2.0 ** -6 and t[0x38] == 1.0 and t[0x39] == 1.125
+    assert t[0x7E] == 448.0 and math.isnan(t[0x7F]) and math.isnan(t[0xFF])
+    assert t[0xB8] == -1.0 and t[0xFE] == -448.0 and math.copysign(1.0, t[0x80]) < 0
+    assert np.all(np.diff(t[0x00:0x7F]) > 0)           # increasing over the positive codes
+    # every code against torch's float8_e4m3fn decoding
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(np.isnan(ref), np.isnan(t))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(ref[fin], t[fin])
+
+
+def pin_e4m3_quantizer(lib):
+    t = O.e4m3_table(lib=lib)
+    codes, vals = _finite_codes(t)
+    pos = np.sort(vals[vals > 0])
+    mids = (pos[:-1] + pos[1:]) / 2                          # exact ties
+    xs = [0.0, -0.0, 2.0 ** -10, 3 * 2.0 ** -10, 2.0 ** -9, 448.0, 460.0, 464.0, 470.0,
+          480.0, 1e4, 1e30]
+    xs += list(pos) + list(mids) + list(mids * (1 + 2.0 ** -7)) + list(mids * (1 - 2.0 ** -7))
+    gen = torch.Generator().manual_seed(81)
+    xs += list((torch.randn(2000, generator=gen) * 40).tolist())
+    xs += list((torch.randn(500, generator=gen) * 0.01).tolist())
+    x = torch.tensor(xs + [-v for v in xs], dtype=torch.float64).to(torch.bfloat16)
+    for scale in (1.0, 0.75, 3.0, 2.0 ** -5):
+        got = O.quantize_e4m3(_bits(x), scale, lib=lib)
+        inv = np.float32(1.0) / np.float32(scale)
+        v = (x.float().numpy() * inv).astype(np.float32)      # binary32 product
+        want = np.array([_nearest_code(float(a), codes, vals) for a in v], np.uint8)
+        assert np.array_equal(got, want), f"scale {scale}"
+        # torch's conversion agrees wherever no saturation is involved
+        inr = np.abs(v) <= 448.0
+        tc = torch.from_numpy(v[inr]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(tc, got[inr]), f"torch scale {scale}"
+
+
+def pin_store_fp8(lib):
+    gen = torch.Generator().manual_seed(82)
+    NB, bs, Hkv = 3, 256, 2
+    T = 5
+    k = _bf16((T, Hkv, D), gen, 30.0)
+    v = _bf16((T, Hkv, D), gen, 0.2)
+    kc = np.zeros((NB, bs, Hkv, D), np.uint8)
+    vc = np.zeros((NB, bs, Hkv, D), np.uint8)
+    slots = np.array([0, 255, 256, -1, 3 * 256 - 1], np.int32)
+    O.store_fp8(_bits(k), _bits(v), kc, vc, slots, 0.5, 0.01, lib=lib)
+    kq = O.quantize_e4m3(_bits(k), 0.5, lib=lib)
+    vq = O.quantize_e4m3(_bits(v), 0.01, lib=lib)
+    flat_k, flat_v = kc.reshape(NB * bs, Hkv, D), vc.reshape(NB * bs, Hkv, D)
+    for t, s_ in enumerate(slots):
+        if s_ < 0:
+            continue
+        assert np.array_equal(flat_k[s_], kq[t]) and np.array_equal(flat_v[s_], vq[t])
+    written = {int(s_) for s_ in slots if s_ >= 0}
+    for s_ in range(NB * bs):
+        if s_ not in written:
+            assert not flat_k[s_].any() and not flat_v[s_].any()
+    bad = np.array([0, 3 * 256], np.int32)
+    try:
+        O.store_fp8(_bits(k[:2]), _bits(v[:2]), kc, vc, bad, 1.0, 1.0, lib=lib)
+        raise AssertionError("out-of-range slot accepted")
+    except O.OracleError:
+        pass
+
+
+def pin_decode_fp8_equals_bf16(lib):
+    # a pool of random codes; its values times power-of-two scales are exact in
+    # bf16, so the bf16 decode of that pool must give the same doubles
+    t = O.e4m3_table(lib=lib)
+    gen = torch.Generator().manual_seed(83)
+    NB, bs, Hkv, Hq = 4, 256, 2, 4
+    kc = torch.randint(0, 256, (NB, bs, Hkv, D), generator=gen, dtype=torch.int64).numpy()
+    vc = torch.randint(0, 256, (NB, bs, Hkv, D), generator=gen, dtype=torch.int64).numpy()
+    for c in (kc, vc):
+        c[(c & 0x7F) == 0x7F] = 0x3A                        # no NaN codes
+    kc, vc = kc.astype(np.uint8), vc.astype(np.uint8)
+    ks, vs = 0.25, 2.0
+    kb = torch.from_numpy(t[kc] * ks).to(torch.bfloat16)
+    vb = torch.from_numpy(t[vc] * vs).to(torch.bfloat16)
+    assert np.array_equal(kb.double().numpy(), t[kc] * ks)   # exact
+    q = _bf16((3, Hq, D), gen, 0.05)
+    tables = np.array([[2, 0, -1, -1], [1, 3, 0, 2], [3, -1, -1, -1]], np.int32)
+    lens = np.array([300, 1000, 17], np.int32)
+    o8, l8 = O.decode_fp8(_bits(q), kc, vc, tables, lens, D ** -0.5, ks, vs, lib=lib)
+    ob, lb = O.decode(_bits(q), _bits(kb), _bits(vb), tables, lens, D ** -0.5, lib=lib)
+    assert np.array_equal(o8, ob) and np.array_equal(l8, lb)
+
+
 ALL_PINS = [
     pin_store_roundtrip,
     pin_store_rejects,
@@ -446,4 +568,8 @@ ALL_PINS = [
     pin_prefill_one_row_equals_decode,
     pin_prefill_chunk_invariance,
     pin_prefill_rejects_lk_lt_lq,
+    pin_e4m3_table,
+    pin_e4m3_quantizer,
+    pin_store_fp8,
+    pin_decode_fp8_equals_bf16,
 ]

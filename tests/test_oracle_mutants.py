@@ -28,11 +28,11 @@ MUTANTS = [
     ("lse-log2", "*lse = m + std::log(l);", "*lse = m + std::log2(l);"),
     ("no-normalisation", "for (int d = 0; d < D; ++d) out[d] /= l;",
      "for (int d = 0; d < D; ++d) out[d] /= 1.0;"),
-    ("pv-uses-keys", "const uint16_t* v = &V[static_cast<size_t>(j) * D];",
-     "const uint16_t* v = &K[static_cast<size_t>(j) * D];"),
+    ("pv-uses-keys", "out[d] += s[j] * V[static_cast<size_t>(j) * D + d];",
+     "out[d] += s[j] * K[static_cast<size_t>(j) * D + d];"),
     ("gather-swaps-k-v",
-     "std::memcpy(&K[static_cast<size_t>(j) * D], k_cache + src, sizeof(uint16_t) * D);",
-     "std::memcpy(&K[static_cast<size_t>(j) * D], v_cache + src, sizeof(uint16_t) * D);"),
+     "std::memcpy(&K[static_cast<size_t>(j) * D], k_cache + src, sizeof(T) * D);",
+     "std::memcpy(&K[static_cast<size_t>(j) * D], v_cache + src, sizeof(T) * D);"),
     ("store-swaps-block-offset", "const int64_t dst = (blk * block_size + off) * row;",
      "const int64_t dst = (off * num_blocks + blk) * row;"),
     ("store-k-into-v", "std::memcpy(v_cache + dst, v + t * v_tok_stride, sizeof(uint16_t) * row);",
@@ -48,6 +48,21 @@ MUTANTS = [
      "const int64_t o = row * Hq + hh;"),
     ("softmax-max-not-subtracted-from-weights", "s[j] = std::exp(s[j] - m);",
      "s[j] = std::exp(s[j]);"),
+    ("e4m3-bias-8", "mag = std::ldexp(1.0 + m / 8.0, e - 7);",
+     "mag = std::ldexp(1.0 + m / 8.0, e - 8);"),
+    ("e4m3-subnormal-quantum", "mag = std::ldexp(static_cast<double>(m), -9);",
+     "mag = std::ldexp(static_cast<double>(m), -10);"),
+    ("e4m3-ties-away-from-zero", "double m = std::nearbyint(a / quantum);",
+     "double m = std::round(a / quantum);"),
+    ("e4m3-overflow-to-nan", "if (e > 8 || (e == 8 && m > 14.0)) return sign | 0x7E;",
+     "if (e > 8 || (e == 8 && m > 14.0)) return sign | 0x7F;"),
+    ("e4m3-subnormal-binade", "if (e < -6) e = -6;", "if (e < -7) e = -7;"),
+    ("quantize-divides", "const float v = x * inv_scale;", "const float v = x / inv_scale;"),
+    ("fp8-decode-k-uses-v-scale", "K[i] = e4m3_value(Kc[i]) * k_scale;",
+     "K[i] = e4m3_value(Kc[i]) * v_scale;"),
+    ("fp8-store-v-with-k-scale",
+     "v_cache[s * row + i] = quantize(v[t * v_tok_stride + i], v_inv_scale);",
+     "v_cache[s * row + i] = quantize(v[t * v_tok_stride + i], k_inv_scale);"),
 ]
 
 
