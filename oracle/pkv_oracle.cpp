@@ -147,13 +147,15 @@ double e4m3_value(uint8_t code) {
   return sign ? -mag : mag;
 }
 
-// Nearest E4M3 code to v (ties to even), magnitudes beyond 448 saturated to
-// 448, NaN to 0x7F.  All arithmetic below is exact in double.
+// Nearest E4M3 code to v (ties to even), magnitudes beyond 448 (infinity
+// included) saturated to 448, NaN to 0x7F.  All arithmetic below is exact in
+// double.
 uint8_t e4m3_encode(float v) {
   if (std::isnan(v)) return 0x7F;
   const uint8_t sign = std::signbit(v) ? 0x80 : 0x00;
   const double a = std::fabs(static_cast<double>(v));
   if (a == 0.0) return sign;
+  if (std::isinf(a)) return sign | 0x7E;
   int e;       // a = f * 2^(e+1), f in [0.5, 1): the binade of a is 2^e
   std::frexp(a, &e);
   e -= 1;

@@ -56,6 +56,8 @@ MUTANTS = [
      "double m = std::round(a / quantum);"),
     ("e4m3-overflow-to-nan", "if (e > 8 || (e == 8 && m > 14.0)) return sign | 0x7E;",
      "if (e > 8 || (e == 8 && m > 14.0)) return sign | 0x7F;"),
+    ("e4m3-infinity-not-saturated", "if (std::isinf(a)) return sign | 0x7E;",
+     "if (std::isinf(a) && false) return sign | 0x7E;"),
     ("e4m3-subnormal-binade", "if (e < -6) e = -6;", "if (e < -7) e = -7;"),
     ("quantize-divides", "const float v = x * inv_scale;", "const float v = x / inv_scale;"),
     ("fp8-decode-k-uses-v-scale", "K[i] = e4m3_value(Kc[i]) * k_scale;",
