@@ -58,11 +58,12 @@ def _peaks():
 # algorithmic bytes
 
 
-def decode_bytes(w, unique: bool = False) -> int:
+def decode_bytes(w, unique: bool = False, kv_elem_bytes: int = BF16) -> int:
     """K/V of every context token read once (shared prefix once if `unique`),
-    q read, out written, lse written, block-table entries and lengths read."""
+    q read, out written, lse written, block-table entries and lengths read.
+    `kv_elem_bytes`: 2 for the bf16 cache, 1 for the FP8 one."""
     toks = w.unique_kv_tokens if unique else w.kv_tokens
-    kv = toks * w.Hkv * w.D * BF16 * 2
+    kv = toks * w.Hkv * w.D * kv_elem_bytes * 2
     qo = 2 * w.B * w.Hq * w.D * BF16
     lse = w.B * w.Hq * 4
     tables = int(sum(-(-int(L) // w.block_size) for L in w.context_lens)) * 4 + w.B * 4
@@ -578,7 +579,59 @@ def run_extras(pkv, dev, hbm_peak, args):
     del w, q, kc, vc, kn, vn, slots, tables, cq, ck, out, lse
     torch.cuda.empty_cache()
     res["verify-b64-q4"] = run_verify_extra(pkv, dev, hbm_peak, flush, stream)
+    for cfg in (2, 5):
+        e = run_fp8_extra(pkv, dev, hbm_peak, flush, stream, cfg)
+        res[e["workload"]] = e
     return res
+
+
+def run_fp8_extra(pkv, dev, hbm_peak, flush, stream, cfg):
+    """Decode over the FP8 (E4M3) cache: the bf16 pool of a decode workload is
+    quantized once with kv_cache_store_fp8 (per-tensor scales), then
+    paged_decode_attention_fp8 is timed with L2 flushed before each call."""
+    w = W.config_workload(cfg, pool_device=dev)
+    NB, bs = w.num_blocks, w.block_size
+    k8 = torch.empty((NB, bs, w.Hkv, w.D), dtype=torch.uint8, device=dev)
+    v8 = torch.empty_like(k8)
+    ks, vs = 6.0 / 448, 6.0 / 448
+    every = torch.arange(NB * bs, dtype=torch.int32, device=dev)
+    pkv.kv_cache_store_fp8(w.k_cache.view(-1, w.Hkv, w.D), w.v_cache.view(-1, w.Hkv, w.D),
+                           k8, v8, every, ks, vs, stream=stream)
+    del every
+    w.k_cache = w.v_cache = None
+    torch.cuda.empty_cache()
+    q = w.q.to(dev)
+    tables, lens = w.block_tables.to(dev), w.context_lens.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    need = pkv.paged_decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, tables.shape[1])
+    ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+
+    def call():
+        pkv.paged_decode_attention_fp8(q, k8, v8, tables, lens, w.scale, ks, vs, out=out,
+                                       lse=lse, workspace=ws, stream=stream)
+    for _ in range(5):
+        call()
+    times = []
+    for _ in range(30):
+        _flush_l2(flush)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    ms = sorted(x.elapsed_time(y) for x, y in times)
+    med = ms[len(ms) // 2]
+    gbs = decode_bytes(w, kv_elem_bytes=1) / (med / 1e3) / 1e9
+    entry = {"workload": w.name + "-fp8", "median_us": round(med * 1e3, 2),
+             "min_us": round(ms[0] * 1e3, 2), "kv_tokens": w.kv_tokens,
+             "kv_tokens_per_s": round(w.kv_tokens / (med / 1e3), 1), "GB/s": round(gbs, 1),
+             "frac_of_peak": round(gbs / hbm_peak, 4),
+             "note": "E4M3 K/V, one byte per element (GB/s counts those bytes)"}
+    del w, q, k8, v8, tables, lens, out, lse, ws
+    torch.cuda.empty_cache()
+    return entry
 
 
 def run_verify_extra(pkv, dev, hbm_peak, flush, stream):

@@ -261,6 +261,37 @@ int paged_decode_attention_multiquery(void* out, float* lse, const void* q,
                                       float scale, void* workspace, size_t workspace_bytes,
                                       int num_splits, pkv_stream_t stream);
 
+/* FP8 KV cache.  The pages name quantized KV only as "compressed transfers"
+ * ("Why Understand Inference Engine Architecture?", Tensor Parallelism
+ * Optimization); the format here is this library's choice: OCP FP8 E4M3 (1
+ * sign, 4 exponent bits with bias 7, 3 mantissa bits, subnormals, no infinity,
+ * largest finite 448), one byte per element, with one scale per tensor.  A pool
+ * is bytes [num_blocks, block_size, Hkv, D], 16-byte aligned; an element's
+ * value is code value * scale.
+ *
+ * kv_cache_store_fp8 — kv_cache_store into FP8 pools: element x of k (v) is
+ * stored as the E4M3 code nearest to fp32(x * fp32(1 / k_scale)) (v_scale for
+ * v), ties to the even code, magnitudes past 448 saturated to 448.  Slot rules,
+ * layouts of k / v and errors as kv_cache_store; k_scale and v_scale must be
+ * finite and > 0 (else PKV_ERR_ARG).  Rows whose start is 16-byte aligned are
+ * converted 16 elements at a time, others element by element. */
+int kv_cache_store_fp8(const void* k, const void* v, int64_t k_tok_stride,
+                       int64_t v_tok_stride, void* k_cache, void* v_cache,
+                       const int32_t* slot_mapping, int64_t T, int Hkv, int D, int block_size,
+                       int64_t num_blocks, float k_scale, float v_scale, pkv_stream_t stream);
+
+/* paged_decode_attention_fp8 — paged_decode_attention over FP8 pools: key j is
+ * code value * k_scale and value j is code value * v_scale.  Half the bytes of
+ * the bf16 cache per token.  Arguments, workspace (paged_decode_workspace_bytes
+ * of the same shapes), results and errors as paged_decode_attention; k_scale
+ * and v_scale must be finite and > 0. */
+int paged_decode_attention_fp8(void* out, float* lse, const void* q, const void* k_cache,
+                               const void* v_cache, const int32_t* block_tables,
+                               int max_blocks_per_seq, const int32_t* context_lens, int B,
+                               int Hq, int Hkv, int D, int block_size, int64_t num_blocks,
+                               float scale, float k_scale, float v_scale, void* workspace,
+                               size_t workspace_bytes, int num_splits, pkv_stream_t stream);
+
 /* paged_prefill_attention — causal prefill / chunked prefill with a prefix
  * cache: "During prefill with prefix cache, gathers cached K/V from the paged
  * cache and concatenates with newly computed ones" (Nano-vLLM System

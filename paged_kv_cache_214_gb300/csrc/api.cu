@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <mutex>
 
 #include "pkv_internal.h"
@@ -58,20 +59,24 @@ unsigned* device_error_word() {
   return g_err_ptr[dev];
 }
 
+// The driver's tensor-map encoder, looked up once.
+bool encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return true;
+}
+
 bool encode_pool_map(CUtensorMap* map, const void* base, int64_t num_slots, int Hkv,
                      int box_rows, int box_heads) {
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_encode) {
-      void* fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                           cudaEnableDefault, &q) != cudaSuccess ||
-          q != cudaDriverEntryPointSuccess || !fn)
-        return false;
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-  }
+  if (!encoder()) return false;
   // [slots, Hkv, D] with D innermost; a box is 64 dims (128 B, the swizzle
   // span) x box_heads heads x box_rows consecutive slots.
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(Hkv),
@@ -82,6 +87,23 @@ bool encode_pool_map(CUtensorMap* map, const void* base, int64_t num_slots, int 
                              static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool encode_pool_map_u8(CUtensorMap* map, const void* base, int64_t num_slots, int Hkv,
+                        int box_rows) {
+  if (!encoder()) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(Hkv),
+                              static_cast<cuuint64_t>(num_slots)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim),
+                                 static_cast<cuuint64_t>(Hkv) * kHeadDim};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), 1,
+                             static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base),
                               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -120,6 +142,32 @@ extern "C" int kv_cache_store(const void* k, const void* v, int64_t k_tok_stride
   StoreArgs a{k, v, k_tok_stride, v_tok_stride, k_cache, v_cache, slot_mapping, T,
               static_cast<int>(row), num_blocks * block_size};
   return launch_store(a, err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+namespace {
+bool valid_scale(float s) { return std::isfinite(s) && s > 0.f; }
+}  // namespace
+
+extern "C" int kv_cache_store_fp8(const void* k, const void* v, int64_t k_tok_stride,
+                                  int64_t v_tok_stride, void* k_cache, void* v_cache,
+                                  const int32_t* slot_mapping, int64_t T, int Hkv, int D,
+                                  int block_size, int64_t num_blocks, float k_scale,
+                                  float v_scale, pkv_stream_t stream) {
+  if (T < 0 || !valid_scale(k_scale) || !valid_scale(v_scale)) return PKV_ERR_ARG;
+  int st = check_pool(Hkv, D, block_size, num_blocks);
+  if (st) return st;
+  if (T == 0) return PKV_OK;
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_ARG;
+  const int64_t row = static_cast<int64_t>(Hkv) * D;
+  if (k_tok_stride < row || v_tok_stride < row) return PKV_ERR_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ARG;
+  unsigned* err = device_error_word();
+  if (!err) return PKV_ERR_LAUNCH;
+  StoreArgs a{k, v, k_tok_stride, v_tok_stride, k_cache, v_cache, slot_mapping, T,
+              static_cast<int>(row), num_blocks * block_size};
+  // the quantizer multiplies by the binary32 reciprocal of each scale
+  const float k_inv = 1.0f / k_scale, v_inv = 1.0f / v_scale;
+  return launch_store_fp8(a, k_inv, v_inv, err, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int kv_cache_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_blocks,
@@ -249,6 +297,41 @@ extern "C" int paged_decode_attention_multiquery(
   if (!err) return PKV_ERR_LAUNCH;
   DecodeArgs a{out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                B, Hq, Hkv, num_blocks, scale, workspace, workspace_bytes, num_splits, 0, q_len};
+  return launch_decode(a, plan, err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int paged_decode_attention_fp8(void* out, float* lse, const void* q,
+                                          const void* k_cache, const void* v_cache,
+                                          const int32_t* block_tables, int max_blocks_per_seq,
+                                          const int32_t* context_lens, int B, int Hq, int Hkv,
+                                          int D, int block_size, int64_t num_blocks, float scale,
+                                          float k_scale, float v_scale, void* workspace,
+                                          size_t workspace_bytes, int num_splits,
+                                          pkv_stream_t stream) {
+  if (B < 0 || Hq <= 0 || max_blocks_per_seq < 0 || num_splits < 0) return PKV_ERR_ARG;
+  if (!valid_scale(k_scale) || !valid_scale(v_scale)) return PKV_ERR_ARG;
+  int st = check_pool(Hkv, D, block_size, num_blocks);
+  if (st) return st;
+  if (Hq % Hkv) return PKV_ERR_SHAPE;
+  if (B == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !context_lens) return PKV_ERR_ARG;
+  if (max_blocks_per_seq > 0 && !block_tables) return PKV_ERR_ARG;
+  if (num_blocks == 0 && max_blocks_per_seq > 0) return PKV_ERR_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_ARG;
+  DecodePlan plan;
+  st = plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), 0, &plan);
+  if (st) return st;
+  if (plan.workspace_bytes) {
+    if (!workspace || workspace_bytes < plan.workspace_bytes ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+      return PKV_ERR_WORKSPACE;
+  }
+  unsigned* err = device_error_word();
+  if (!err) return PKV_ERR_LAUNCH;
+  DecodeArgs a{out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+               B, Hq, Hkv, num_blocks, scale, workspace, workspace_bytes, num_splits, 0, 1,
+               1, k_scale, v_scale};
   return launch_decode(a, plan, err, reinterpret_cast<cudaStream_t>(stream));
 }
 

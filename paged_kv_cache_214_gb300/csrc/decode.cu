@@ -75,6 +75,7 @@ struct DecodeParams {
   // kv*(g/q_len) + (v%g)%(g/q_len), with g = Hq/Hkv.  q_len = 1 is plain decode.
   int B, Hq, Hkv, maxblk, num_splits, split_blocks, head_groups;
   int q_len, Hq_phys;
+  float k_scale, v_scale;   // FP8 pools: element value = code value * scale
   int64_t num_blocks;
   float scale_log2;
   // Shared prefix (0 = none): every sequence's first prefix_tokens tokens are
@@ -125,8 +126,24 @@ __device__ __forceinline__ void merge_row(const float* lrow, const float* orow, 
   if (lse && lane == 0) *lse = (mx + __log2f(sum)) * 0.69314718055994530942f;
 }
 
-template <int G>
+// Pipeline geometry per element type.  bf16: 3 stages of 64 tokens, each
+// operand two 64-dim boxes (four copies per stage, one per warp).  FP8 (E4M3,
+// one byte per element): a row of 128 dims is one 128-byte box, so a stage of
+// 64 tokens holds half the bytes; 6 stages keep the same bytes in flight, and
+// warps 0 and 1 issue the K and the V copy of each stage.
+template <bool kFp8>
+struct Geo {
+  static constexpr int kStagesN = kFp8 ? 6 : 3;
+  static constexpr int kOpBytes = kTile * (kFp8 ? 128 : 256);  // one of K or V for a stage
+  static constexpr int kStageB = 2 * kOpBytes;
+  static constexpr int kIssuers = kFp8 ? 2 : 4;
+};
+static_assert(Geo<false>::kStagesN == kStages && Geo<false>::kStageB == kStageBytes, "geometry");
+
+template <int G, bool kFp8 = false>
 struct SmemLayout {
+  static constexpr int kStages = Geo<kFp8>::kStagesN;
+  static constexpr int kStageBytes = Geo<kFp8>::kStageB;
   static constexpr int kMergeO = kStages * kStageBytes;                      // [4][G][128] f32
   static constexpr int kMergeM = kMergeO + kConsumerWarps * G * 128 * 4;     // [4][G]
   static constexpr int kMergeL = kMergeM + kConsumerWarps * G * 4;           // [4][G]
@@ -144,12 +161,17 @@ __device__ __forceinline__ float rescale(float m, float mn) {
 }
 
 // kMQ: several query positions per sequence (q_len > 1); plain decode
-// compiles without the per-row key limits.
-template <int G, int KVH, bool kMQ>
+// compiles without the per-row key limits.  kFp8: E4M3 pools (KVH = 1 only).
+template <int G, int KVH, bool kMQ, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 2)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
-  using L = SmemLayout<G>;
+  static_assert(!kFp8 || KVH == 1, "FP8 pools are read one kv head per block");
+  using L = SmemLayout<G, kFp8>;
+  constexpr int kStagesN = Geo<kFp8>::kStagesN;
+  constexpr int kStageB = Geo<kFp8>::kStageB;
+  constexpr int kOpBytes = Geo<kFp8>::kOpBytes;
+  constexpr int kIssuers = Geo<kFp8>::kIssuers;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -160,7 +182,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   volatile int* flags = reinterpret_cast<volatile int*>(smem + L::kFlags);
   const uint32_t bars = smem_addr(smem + L::kBars);
   auto full_bar = [&](int s) { return bars + 8u * s; };
-  auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
+  auto empty_bar = [&](int s) { return bars + 8u * (kStagesN + s); };
 
   // KVH kv heads per block: each pipeline stage holds kTT tokens x KVH heads
   // (so a token contributes one contiguous KVH x 256-byte chunk), and
@@ -249,21 +271,31 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   // warps have released the stage.
   const uint64_t policy = l2_policy_evict_first();
   auto issue = [&](int it) {
-    const int s = it % kStages;
+    const int s = it % kStagesN;
     const int tok = tok_begin + it * kTT;
     const int slot = sblk[tok / kBlockSize - blk_begin] * kBlockSize + tok % kBlockSize;
-    const uint32_t dst = smem_addr(smem + s * kStageBytes) + warp * kHalfBytes;
-    mbar_arrive_expect_tx(full_bar(s), kHalfBytes);
-    if (warp < 2)
-      tma_load_3d_hint(dst, &kmap, full_bar(s), (warp & 1) * 64, kvh0, slot, policy);
-    else
-      tma_load_3d_hint(dst, &vmap, full_bar(s), (warp & 1) * 64, kvh0, slot, policy);
+    if constexpr (kFp8) {
+      // warp 0: the K tile, warp 1: the V tile (one 128-byte-wide box each)
+      const uint32_t dst = smem_addr(smem + s * kStageB) + warp * kOpBytes;
+      mbar_arrive_expect_tx(full_bar(s), kOpBytes);
+      if (warp == 0)
+        tma_load_3d_hint(dst, &kmap, full_bar(s), 0, kvh0, slot, policy);
+      else
+        tma_load_3d_hint(dst, &vmap, full_bar(s), 0, kvh0, slot, policy);
+    } else {
+      const uint32_t dst = smem_addr(smem + s * kStageB) + warp * kHalfBytes;
+      mbar_arrive_expect_tx(full_bar(s), kHalfBytes);
+      if (warp < 2)
+        tma_load_3d_hint(dst, &kmap, full_bar(s), (warp & 1) * 64, kvh0, slot, policy);
+      else
+        tma_load_3d_hint(dst, &vmap, full_bar(s), (warp & 1) * 64, kvh0, slot, policy);
+    }
     atomicMax(const_cast<int*>(flags + 2), it + 1);
   };
   if (warp == 0) {
     if (lane == 0) {
-      for (int s = 0; s < kStages; ++s) {
-        mbar_init(full_bar(s), kConsumerWarps);   // one arrival per quarter
+      for (int s = 0; s < kStagesN; ++s) {
+        mbar_init(full_bar(s), kIssuers);         // one arrival per issuing warp
         mbar_init(empty_bar(s), kConsumerWarps);
       }
       flags[0] = 0;  // abort
@@ -283,8 +315,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     }
   }
   __syncthreads();
-  if (lane == 0)
-    for (int it = 0; it < kStages && it < n_tiles; ++it) issue(it);
+  if (lane == 0 && warp < kIssuers)
+    for (int it = 0; it < kStagesN && it < n_tiles; ++it) issue(it);
 
   {
     // ------------------------------------------------------------ consumers
@@ -296,14 +328,17 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     // stage, held in shared-memory row token*KVH + my_hh (128-byte rows).
     // q (pre-scaled into base-2 units) and the running output, as fp32 pairs:
     // pair i < 4 covers dims 8j+2i, 8j+2i+1; pair i >= 4 covers 64+8j+2(i-4), +1.
+    // (FP8: lane j owns dims [16j, 16j+16) instead, pair i = dims 16j+2i, +1,
+    // and q also carries the K scale.)
     f32x2 q2[G][8];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const __nv_bfloat16* qp = p.q + phys_row(qhead(my_hh, h)) * kHeadDim;
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(qp + 8 * j));
-      const uint4 c = __ldg(reinterpret_cast<const uint4*>(qp + 64 + 8 * j));
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(qp + (kFp8 ? 16 * j : 8 * j)));
+      const uint4 c = __ldg(reinterpret_cast<const uint4*>(qp + (kFp8 ? 16 * j + 8 : 64 + 8 * j)));
       const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-      const f32x2 sc2 = pack2(p.scale_log2, p.scale_log2);
+      const float qs = kFp8 ? p.scale_log2 * p.k_scale : p.scale_log2;
+      const f32x2 sc2 = pack2(qs, qs);
 #pragma unroll
       for (int i = 0; i < 8; ++i) q2[h][i] = mul2(bf16x2_to_f32x2(w[i]), sc2);
     }
@@ -320,16 +355,16 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     }
 
     for (int it = 0; it < n_tiles; ++it) {
-      const int s = it % kStages;
+      const int s = it % kStagesN;
       if (flags[0]) break;
-      if (!mbar_wait(full_bar(s), (it / kStages) & 1)) {
+      if (!mbar_wait(full_bar(s), (it / kStagesN) & 1)) {
         record_error(p.err, kErrTimeout);
         flags[0] = 1;
         break;
       }
       const int n_valid = min(kTT, tok_end - (tok_begin + it * kTT));
-      const uint32_t kb = smem_addr(smem + s * kStageBytes);
-      const uint32_t vb = kb + kOperandBytes;
+      const uint32_t kb = smem_addr(smem + s * kStageB);
+      const uint32_t vb = kb + kOpBytes;
 
       // scores of this group's four rows of the tile, base-2 units
       float sc[4][G];
@@ -338,12 +373,22 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         const int t = 4 * (r * kWPH + my_wl) + grp;
         const int srow = t * KVH + my_hh;
         const uint32_t off = srow * 128 + ((j ^ (srow & 7)) << 4);
-        const uint4 k0 = lds128(kb + off);
-        const uint4 k1 = lds128(kb + kHalfBytes + off);
-        const uint32_t w[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
         f32x2 kf[8];
+        if constexpr (kFp8) {
+          const uint4 k0 = lds128(kb + off);
+          const uint32_t w[4] = {k0.x, k0.y, k0.z, k0.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) kf[i] = bf16x2_to_f32x2(w[i]);
+          for (int i = 0; i < 4; ++i) {
+            kf[2 * i] = e4m3x2_to_f32x2(static_cast<uint16_t>(w[i] & 0xFFFFu));
+            kf[2 * i + 1] = e4m3x2_to_f32x2(static_cast<uint16_t>(w[i] >> 16));
+          }
+        } else {
+          const uint4 k0 = lds128(kb + off);
+          const uint4 k1 = lds128(kb + kHalfBytes + off);
+          const uint32_t w[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) kf[i] = bf16x2_to_f32x2(w[i]);
+        }
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           f32x2 a0 = mul2(q2[h][0], kf[0]);
@@ -388,12 +433,22 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         if (t < n_valid) {
           const int srow = t * KVH + my_hh;
           const uint32_t off = srow * 128 + ((j ^ (srow & 7)) << 4);
-          const uint4 v0 = lds128(vb + off);
-          const uint4 v1 = lds128(vb + kHalfBytes + off);
-          const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
           f32x2 vf[8];
+          if constexpr (kFp8) {
+            const uint4 v0 = lds128(vb + off);
+            const uint32_t w[4] = {v0.x, v0.y, v0.z, v0.w};
 #pragma unroll
-          for (int i = 0; i < 8; ++i) vf[i] = bf16x2_to_f32x2(w[i]);
+            for (int i = 0; i < 4; ++i) {
+              vf[2 * i] = e4m3x2_to_f32x2(static_cast<uint16_t>(w[i] & 0xFFFFu));
+              vf[2 * i + 1] = e4m3x2_to_f32x2(static_cast<uint16_t>(w[i] >> 16));
+            }
+          } else {
+            const uint4 v0 = lds128(vb + off);
+            const uint4 v1 = lds128(vb + kHalfBytes + off);
+            const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) vf[i] = bf16x2_to_f32x2(w[i]);
+          }
 #pragma unroll
           for (int h = 0; h < G; ++h) {
             const f32x2 p2 = pack2(sc[r][h], sc[r][h]);
@@ -405,9 +460,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(empty_bar(s));
-        if (it + kStages < n_tiles && !flags[0]) {
-          if (mbar_wait(empty_bar(s), (it / kStages) & 1)) {
-            issue(it + kStages);
+        if (warp < kIssuers && it + kStagesN < n_tiles && !flags[0]) {
+          if (mbar_wait(empty_bar(s), (it / kStagesN) & 1)) {
+            issue(it + kStagesN);
           } else {
             record_error(p.err, kErrTimeout);
             flags[0] = 1;
@@ -449,8 +504,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         float* dst = merge_o + (warp * G + h) * kHeadDim;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          dst[8 * j + i] = o[h][i];
-          dst[64 + 8 * j + i] = o[h][8 + i];
+          dst[(kFp8 ? 16 * j : 8 * j) + i] = o[h][i];
+          dst[(kFp8 ? 16 * j + 8 : 64 + 8 * j) + i] = o[h][8 + i];
         }
         if (j == 0) {
           merge_m[warp * G + h] = m[h];
@@ -465,10 +520,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   // block's shared memory can be released.
   if (flags[0] && tid == 0) {
     const int issued = flags[2];
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kStagesN; ++s) {
       int last = -1;
-      for (int it = s; it < issued; it += kStages) last = it;
-      if (last >= 0) (void)mbar_wait(full_bar(s), (last / kStages) & 1);
+      for (int it = s; it < issued; it += kStagesN) last = it;
+      if (last >= 0) (void)mbar_wait(full_bar(s), (last / kStagesN) & 1);
     }
   }
 
@@ -490,7 +545,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     }
     // a split may hold no key a row can see (later query positions only):
     // its partial is then 0 with log2-sum-exp -inf, which the merge ignores
-    const float on = Ls > 0.f ? Os / Ls : 0.f;
+    float on = Ls > 0.f ? Os / Ls : 0.f;
+    if constexpr (kFp8) on *= p.v_scale;
     const float lse2 = M + __log2f(Ls);
     const int64_t row = static_cast<int64_t>(b) * p.Hq + qhead(hh, h);
     if (single) {
@@ -531,23 +587,23 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   if (tid == 0) *counter = 0u;  // ready for the next call
 }
 
-template <int G, int KVH, bool kMQ>
+template <int G, int KVH, bool kMQ, bool kFp8 = false>
 int launch_g(const DecodeArgs& a, const DecodePlan& plan, const DecodeParams& prm,
              const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t stream) {
-  using L = SmemLayout<G>;
+  using L = SmemLayout<G, kFp8>;
   static_assert(L::kBytes <= 113 * 1024, "two blocks per SM must fit");
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(paged_decode_kernel<G, KVH, kMQ>,
+    if (cudaFuncSetAttribute(paged_decode_kernel<G, KVH, kMQ, kFp8>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::kBytes) != cudaSuccess)
       return PKV_ERR_LAUNCH;
     attr_set[dev] = true;
   }
   dim3 grid(plan.num_splits, (a.Hkv / KVH) * plan.head_groups, a.B);
-  paged_decode_kernel<G, KVH, kMQ><<<grid, kThreads, L::kBytes, stream>>>(km, vm, prm);
+  paged_decode_kernel<G, KVH, kMQ, kFp8><<<grid, kThreads, L::kBytes, stream>>>(km, vm, prm);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }
 
@@ -633,9 +689,14 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
   CUtensorMap km, vm;
   const int64_t slots = a.num_blocks * kBlockSize;
   const int kvh = plan.kv_per_cta;
-  if (!encode_pool_map(&km, a.k_cache, slots, a.Hkv, kTile / kvh, kvh) ||
-      !encode_pool_map(&vm, a.v_cache, slots, a.Hkv, kTile / kvh, kvh))
+  if (a.fp8) {
+    if (!encode_pool_map_u8(&km, a.k_cache, slots, a.Hkv, kTile) ||
+        !encode_pool_map_u8(&vm, a.v_cache, slots, a.Hkv, kTile))
+      return PKV_ERR_ARG;
+  } else if (!encode_pool_map(&km, a.k_cache, slots, a.Hkv, kTile / kvh, kvh) ||
+             !encode_pool_map(&vm, a.v_cache, slots, a.Hkv, kTile / kvh, kvh)) {
     return PKV_ERR_ARG;
+  }
   DecodeParams prm;
   prm.out = static_cast<__nv_bfloat16*>(a.out);
   prm.lse = a.lse;
@@ -647,6 +708,8 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
   prm.Hq = a.Hq * a.q_len;   // virtual heads (see DecodeParams)
   prm.Hq_phys = a.Hq;
   prm.q_len = a.q_len;
+  prm.k_scale = a.k_scale;
+  prm.v_scale = a.v_scale;
   prm.Hkv = a.Hkv;
   prm.maxblk = a.max_blocks_per_seq;
   prm.num_splits = plan.num_splits;
@@ -677,6 +740,13 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
     prm.ws_o = nullptr;
     prm.ws_lse = nullptr;
     prm.ws_count = nullptr;
+  }
+  if (a.fp8) {
+    switch (plan.heads_per_cta) {
+      case 4: return launch_g<4, 1, false, true>(a, plan, prm, km, vm, stream);
+      case 2: return launch_g<2, 1, false, true>(a, plan, prm, km, vm, stream);
+      default: return launch_g<1, 1, false, true>(a, plan, prm, km, vm, stream);
+    }
   }
   switch (plan.heads_per_cta) {
     case 4:

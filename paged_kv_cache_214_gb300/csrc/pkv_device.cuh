@@ -445,4 +445,28 @@ __device__ __forceinline__ void tmem_st16x128_x16(uint32_t taddr, const uint32_t
                : "memory");
 }
 
+
+// ---------------------------------------------------------------- FP8 (E4M3)
+
+// Two floats -> two E4M3 codes, round to nearest even, magnitudes past 448
+// saturated to 448; `lo` lands in the low byte.
+__device__ __forceinline__ uint16_t e4m3x2_from_f32(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two E4M3 codes (element 0 in the low byte) -> (element 0, element 1) in
+// fp32; exact (every E4M3 value is an fp16 value).
+__device__ __forceinline__ f32x2 e4m3x2_to_f32x2(uint16_t codes) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(codes));
+  float a, b;
+  asm("{\n\t.reg .b16 x, y;\n\tmov.b32 {x, y}, %2;\n\tcvt.f32.f16 %0, x;\n\t"
+      "cvt.f32.f16 %1, y;\n\t}"
+      : "=f"(a), "=f"(b)
+      : "r"(h));
+  return pack2(a, b);
+}
+
 }  // namespace pkv

@@ -28,6 +28,10 @@ unsigned* device_error_word();
 // box = {64 elements of D, box_heads heads, box_rows slots}, 128-byte swizzle.
 bool encode_pool_map(CUtensorMap* map, const void* base, int64_t num_slots, int Hkv,
                      int box_rows, int box_heads = 1);
+// The same for an FP8 pool [slots, Hkv, 128] of bytes: a box is one 128-byte
+// row (all 128 dims) of one kv head x box_rows consecutive slots.
+bool encode_pool_map_u8(CUtensorMap* map, const void* base, int64_t num_slots, int Hkv,
+                        int box_rows);
 
 struct StoreArgs {
   const void* k;
@@ -42,6 +46,9 @@ struct StoreArgs {
   int64_t num_slots;
 };
 int launch_store(const StoreArgs& a, unsigned* err, cudaStream_t stream);
+// FP8 (E4M3) pool: k_inv / v_inv are 1/scale rounded to fp32.
+int launch_store_fp8(const StoreArgs& a, float k_inv, float v_inv, unsigned* err,
+                     cudaStream_t stream);
 int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst,
                        int n_pairs, int64_t block_bytes, int64_t num_blocks, unsigned* err,
                        cudaStream_t stream);
@@ -63,6 +70,8 @@ struct DecodeArgs {
   int num_splits;  // as requested (0 = automatic)
   int prefix_tokens;  // shared prefix handled by a separate pass (0 = none)
   int q_len = 1;      // query positions per sequence (several: speculative verify)
+  int fp8 = 0;        // pools hold E4M3 codes: element = code value * k_scale / v_scale
+  float k_scale = 1.f, v_scale = 1.f;
 };
 
 // Split plan of one decode call.

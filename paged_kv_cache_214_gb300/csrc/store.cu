@@ -80,6 +80,56 @@ kv_copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
   }
 }
 
+// FP8 store: every bf16 element x of a token row becomes the E4M3 code of
+// x * inv_scale (inv_scale = 1/scale rounded to fp32 by the host; the product
+// rounded to fp32, then to the nearest code, ties to even, saturating at 448).
+// VEC: 16 elements per thread (two 16-byte loads, one 16-byte store).
+template <bool VEC>
+__global__ void __launch_bounds__(kStoreThreads)
+kv_store_fp8_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+                    int64_t k_stride, int64_t v_stride, uint8_t* __restrict__ k_cache,
+                    uint8_t* __restrict__ v_cache, const int32_t* __restrict__ slots, int64_t T,
+                    int row_elems, int64_t num_slots, float k_inv, float v_inv, unsigned* err) {
+  constexpr int kPer = VEC ? 16 : 1;
+  const int pieces = row_elems / kPer;
+  const int64_t per_token = 2 * static_cast<int64_t>(pieces);
+  const int64_t total = T * per_token;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const int64_t t = i / per_token;
+    const int rem = static_cast<int>(i - t * per_token);
+    const int which = rem >= pieces;  // 0 = K, 1 = V
+    const int piece = rem - which * pieces;
+    const int64_t s = __ldg(slots + t);
+    if (s < 0) continue;
+    if (s >= num_slots) {
+      if (piece == 0 && which == 0) record_error(err, kErrIndex);
+      continue;
+    }
+    const uint16_t* src = (which ? v + t * v_stride : k + t * k_stride) + piece * kPer;
+    uint8_t* dst = (which ? v_cache : k_cache) + s * row_elems + piece * kPer;
+    const float inv = which ? v_inv : k_inv;
+    if constexpr (VEC) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(src));
+      const uint4 b = __ldg(reinterpret_cast<const uint4*>(src) + 1);
+      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t c0 = e4m3x2_from_f32(bf16lo(w[2 * j]) * inv, bf16hi(w[2 * j]) * inv);
+        const uint32_t c1 =
+            e4m3x2_from_f32(bf16lo(w[2 * j + 1]) * inv, bf16hi(w[2 * j + 1]) * inv);
+        o[j] = c0 | (c1 << 16);
+      }
+      *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+      const float x = __uint_as_float(static_cast<uint32_t>(__ldg(src)) << 16);
+      *dst = static_cast<uint8_t>(e4m3x2_from_f32(x * inv, 0.f) & 0xFFu);
+    }
+  }
+}
+
 }  // namespace
 
 int launch_copy_blocks(void* k_cache, void* v_cache, const int32_t* src, const int32_t* dst,
@@ -124,6 +174,35 @@ int launch_store(const StoreArgs& a, unsigned* err, cudaStream_t stream) {
     kv_store_kernel<false><<<static_cast<unsigned>(blocks), kStoreThreads, 0, stream>>>(
         k, v, a.k_tok_stride, a.v_tok_stride, kc, vc, a.slot_mapping, a.T, a.row_elems,
         a.num_slots, err);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+}
+
+int launch_store_fp8(const StoreArgs& a, float k_inv, float v_inv, unsigned* err,
+                     cudaStream_t stream) {
+  if (a.T == 0) return PKV_OK;
+  const bool vec = (reinterpret_cast<uintptr_t>(a.k) % 16 == 0) &&
+                   (reinterpret_cast<uintptr_t>(a.v) % 16 == 0) &&
+                   ((a.k_tok_stride * 2) % 16 == 0) && ((a.v_tok_stride * 2) % 16 == 0) &&
+                   (a.row_elems % 16 == 0);
+  const int pieces = vec ? a.row_elems / 16 : a.row_elems;
+  const int64_t total = a.T * 2 * static_cast<int64_t>(pieces);
+  int sms = device_sm_count();
+  if (sms <= 0) sms = 148;
+  int64_t blocks = (total + kStoreThreads - 1) / kStoreThreads;
+  const int64_t cap = static_cast<int64_t>(sms) * 16;
+  if (blocks > cap) blocks = cap;
+  const auto* k = static_cast<const uint16_t*>(a.k);
+  const auto* v = static_cast<const uint16_t*>(a.v);
+  auto* kc = static_cast<uint8_t*>(a.k_cache);
+  auto* vc = static_cast<uint8_t*>(a.v_cache);
+  if (vec)
+    kv_store_fp8_kernel<true><<<static_cast<unsigned>(blocks), kStoreThreads, 0, stream>>>(
+        k, v, a.k_tok_stride, a.v_tok_stride, kc, vc, a.slot_mapping, a.T, a.row_elems,
+        a.num_slots, k_inv, v_inv, err);
+  else
+    kv_store_fp8_kernel<false><<<static_cast<unsigned>(blocks), kStoreThreads, 0, stream>>>(
+        k, v, a.k_tok_stride, a.v_tok_stride, kc, vc, a.slot_mapping, a.T, a.row_elems,
+        a.num_slots, k_inv, v_inv, err);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }
 

@@ -76,6 +76,12 @@ def load_library(path: str = LIB_PATH):
         lib.paged_decode_attention_multiquery.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32,
                                                           i32, i32, i32, i64, f32, P, sz, i32, P]
         lib.paged_decode_attention_multiquery.restype = i32
+        lib.kv_cache_store_fp8.argtypes = [P, P, i64, i64, P, P, P, i64, i32, i32, i32, i64,
+                                           f32, f32, P]
+        lib.kv_cache_store_fp8.restype = i32
+        lib.paged_decode_attention_fp8.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32,
+                                                   i32, i64, f32, f32, f32, P, sz, i32, P]
+        lib.paged_decode_attention_fp8.restype = i32
         lib.paged_prefill_attention.argtypes = [P, P, P, P, P, P, i32, P, P, i32, i32, i32,
                                                 i32, i32, i32, i32, i64, f32, P]
         lib.paged_prefill_attention.restype = i32
@@ -230,6 +236,69 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                                       _ptr(context_lens), B, Hq, Hkv, D, bs, NB, float(scale),
                                       _ptr(workspace), ws_bytes, int(num_splits),
                                       _stream(stream)), "paged_decode_attention")
+    return out, lse
+
+
+def _fp8_pool_dims(k_cache: torch.Tensor, v_cache: torch.Tensor):
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _need(t, name, torch.uint8, 4)
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    NB, bs, Hkv, D = k_cache.shape
+    return NB, bs, Hkv, D
+
+
+def kv_cache_store_fp8(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor,
+                       v_cache: torch.Tensor, slot_mapping: torch.Tensor, k_scale: float,
+                       v_scale: float, stream=None) -> None:
+    """Store bf16 k/v [T, Hkv, D] into uint8 E4M3 pools [NB, bs, Hkv, D] (one
+    scale per tensor)."""
+    lib = load_library()
+    NB, bs, Hkv, D = _fp8_pool_dims(k_cache, v_cache)
+    for name, t in (("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, 3, contiguous=False)
+        if t.stride(2) != 1 or t.stride(1) != D:
+            raise ValueError(f"{name}: each token's [Hkv, D] rows must be contiguous")
+    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    T = k.shape[0]
+    _check(lib.kv_cache_store_fp8(_ptr(k), _ptr(v), k.stride(0), v.stride(0), _ptr(k_cache),
+                                  _ptr(v_cache), _ptr(slot_mapping), T, Hkv, D, bs, NB,
+                                  float(k_scale), float(v_scale), _stream(stream)),
+           "kv_cache_store_fp8")
+
+
+def paged_decode_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                               block_tables: torch.Tensor, context_lens: torch.Tensor,
+                               scale: float, k_scale: float, v_scale: float,
+                               out: Optional[torch.Tensor] = None,
+                               lse: Optional[torch.Tensor] = None,
+                               workspace: Optional[torch.Tensor] = None, num_splits: int = 0,
+                               want_lse: bool = True, stream=None
+                               ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Decode over uint8 E4M3 pools; q bf16 [B, Hq, D].  Returns (out bf16
+    [B, Hq, D], lse fp32 [B, Hq] or None)."""
+    lib = load_library()
+    NB, bs, Hkv, D = _fp8_pool_dims(k_cache, v_cache)
+    _need(q, "q", torch.bfloat16, 3)
+    B, Hq, Dq = q.shape
+    if Dq != D:
+        raise ValueError("q head_dim differs from the cache's")
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    maxblk = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    need = paged_decode_workspace_bytes(B, Hq, Hkv, D, maxblk, bs, num_splits)
+    if workspace is None and need:
+        workspace = decode_workspace(need, q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.paged_decode_attention_fp8(
+        _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), maxblk,
+        _ptr(context_lens), B, Hq, Hkv, D, bs, NB, float(scale), float(k_scale), float(v_scale),
+        _ptr(workspace), ws_bytes, int(num_splits), _stream(stream)),
+        "paged_decode_attention_fp8")
     return out, lse
 
 

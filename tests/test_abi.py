@@ -77,6 +77,38 @@ def test_multiquery_host_checks(lib):
     assert lib.paged_decode_multiquery_workspace_bytes(2, 0, 16, 8, 128, 4, 256, 0) == 0
 
 
+def test_fp8_host_checks(lib):
+    s = None
+    st8 = lib.kv_cache_store_fp8
+    dec8 = lib.paged_decode_attention_fp8
+    nan, inf = float("nan"), float("inf")
+    # scales must be finite and > 0, checked before anything else
+    for bad in (0.0, -1.0, nan, inf):
+        assert st8(None, None, 1024, 1024, None, None, None, 4, 8, 128, 256, 4, bad, 1.0,
+                   s) == pkv.PKV_ERR_ARG
+        assert st8(None, None, 1024, 1024, None, None, None, 4, 8, 128, 256, 4, 1.0, bad,
+                   s) == pkv.PKV_ERR_ARG
+        assert dec8(None, None, None, None, None, None, 1, None, 2, 16, 8, 128, 256, 4, 1.0,
+                    bad, 1.0, None, 0, 0, s) == pkv.PKV_ERR_ARG
+        assert dec8(None, None, None, None, None, None, 1, None, 2, 16, 8, 128, 256, 4, 1.0,
+                    1.0, bad, None, 0, 0, s) == pkv.PKV_ERR_ARG
+    # nothing to store / decode is not an error; shapes as for the bf16 calls
+    assert st8(None, None, 1024, 1024, None, None, None, 0, 8, 128, 256, 4, 1.0, 1.0,
+               s) == pkv.PKV_OK
+    assert st8(None, None, 1024, 1024, None, None, None, 4, 8, 64, 256, 4, 1.0, 1.0,
+               s) == pkv.PKV_ERR_SHAPE
+    assert st8(None, None, 1000, 1024, None, None, None, 4, 8, 128, 256, 4, 1.0, 1.0,
+               s) == pkv.PKV_ERR_ARG
+    assert dec8(None, None, None, None, None, None, 1, None, 0, 16, 8, 128, 256, 4, 1.0, 0.5,
+                0.5, None, 0, 0, s) == pkv.PKV_OK
+    assert dec8(None, None, None, None, None, None, 1, None, 2, 12, 8, 128, 256, 4, 1.0, 0.5,
+                0.5, None, 0, 0, s) == pkv.PKV_ERR_SHAPE
+    assert dec8(None, None, None, None, None, None, 1, None, 2, 16, 8, 128, 128, 4, 1.0, 0.5,
+                0.5, None, 0, 0, s) == pkv.PKV_ERR_SHAPE
+    assert dec8(None, None, None, None, None, None, 1, None, 2, 16, 8, 128, 256, 4, 1.0, 0.5,
+                0.5, None, 0, 0, s) == pkv.PKV_ERR_ARG
+
+
 def test_workspace_query_and_split_plan(lib):
     # one split needs no workspace; several need partials + counters
     assert pkv.paged_decode_workspace_bytes(4, 16, 8, 128, 1, 256, 1) == 0
