@@ -804,6 +804,47 @@ def run_shared_prefix_profile(args):
                       "unique_GB/s": round(ub, 1)}), flush=True)
 
 
+def run_fp8_decode_profile(args, long_ctx: bool):
+    """Small-footprint FP8 decode run for ncu: the decode-b64 shapes (2 query
+    heads per kv head) or, with `long_ctx`, 8 sequences of 32k-64k tokens with
+    4 query heads per kv head; pools quantized once with kv_cache_store_fp8."""
+    from paged_kv_cache_214_gb300 import pkv
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if long_ctx:
+        lens = W._uniform_ints(32768, 65536, 8, W.seed_for(5))
+        Hq, name = 32, "long-decode-b8-fp8-trimmed"
+    else:
+        lens = W._uniform_ints(512, 4096, 64, W.seed_for(2))
+        Hq, name = 16, "decode-b64-fp8"
+    nblk = sum(-(-L // W.BLOCK_SIZE) for L in lens)
+    w = W.make_decode(lens, Hq, 8, nblk, W.seed_for(2), name=name, store_new_token=False,
+                      pool_device=dev)
+    k8 = torch.empty((nblk, w.block_size, w.Hkv, w.D), dtype=torch.uint8, device=dev)
+    v8 = torch.empty_like(k8)
+    ks = vs = 6.0 / 448
+    every = torch.arange(nblk * w.block_size, dtype=torch.int32, device=dev)
+    pkv.kv_cache_store_fp8(w.k_cache.view(-1, w.Hkv, w.D), w.v_cache.view(-1, w.Hkv, w.D),
+                           k8, v8, every, ks, vs)
+    w.k_cache = w.v_cache = None
+    q, tables, ctx = w.q.to(dev), w.block_tables.to(dev), w.context_lens.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    need = pkv.paged_decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, tables.shape[1])
+    ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        pkv.paged_decode_attention_fp8(q, k8, v8, tables, ctx, w.scale, ks, vs, out=out,
+                                       lse=lse, workspace=ws, stream=stream)
+    for _ in range(args.warmup):
+        call()
+    med, _ = _time_calls(call, args.steps, stream)
+    assert pkv.get_device_error() == pkv.PKV_OK
+    gbs = decode_bytes(w, kv_elem_bytes=1) / (med / 1e3) / 1e9
+    print(json.dumps({"workload": w.name, "us": round(med * 1e3, 2), "GB/s": round(gbs, 1)}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -812,8 +853,9 @@ def main():
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-kernel", choices=["decode", "prefill", "shared-prefix"],
-                    default="decode",
+    ap.add_argument("--profile-kernel", default="decode",
+                    choices=["decode", "prefill", "shared-prefix", "fp8-decode",
+                             "fp8-decode-long"],
                     help="with --profile: which kernel the run exercises")
     ap.add_argument("--profile", action="store_true",
                     help="small-footprint run for ncu: one batch, trimmed pool, "
@@ -830,6 +872,9 @@ def main():
         return
     if args.profile_kernel == "shared-prefix":
         run_shared_prefix_profile(args)
+        return
+    if args.profile_kernel in ("fp8-decode", "fp8-decode-long"):
+        run_fp8_decode_profile(args, args.profile_kernel == "fp8-decode-long")
         return
     if args.impl == "reference":
         res = run_reference(args, world, rank)

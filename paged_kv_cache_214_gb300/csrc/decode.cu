@@ -129,11 +129,11 @@ __device__ __forceinline__ void merge_row(const float* lrow, const float* orow, 
 // Pipeline geometry per element type.  bf16: 3 stages of 64 tokens, each
 // operand two 64-dim boxes (four copies per stage, one per warp).  FP8 (E4M3,
 // one byte per element): a row of 128 dims is one 128-byte box, so a stage of
-// 64 tokens holds half the bytes; 6 stages keep the same bytes in flight, and
+// 64 tokens holds 16 KB; 4 stages (64 KB) let three blocks share an SM, and
 // warps 0 and 1 issue the K and the V copy of each stage.
 template <bool kFp8>
 struct Geo {
-  static constexpr int kStagesN = kFp8 ? 6 : 3;
+  static constexpr int kStagesN = kFp8 ? 4 : 3;
   static constexpr int kOpBytes = kTile * (kFp8 ? 128 : 256);  // one of K or V for a stage
   static constexpr int kStageB = 2 * kOpBytes;
   static constexpr int kIssuers = kFp8 ? 2 : 4;
@@ -318,7 +318,192 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   if (lane == 0 && warp < kIssuers)
     for (int it = 0; it < kStagesN && it < n_tiles; ++it) issue(it);
 
-  {
+  if constexpr (kFp8) {
+    // ---------------------------------------------- consumers, E4M3 pools
+    // Both contractions run on the warp-level tensor-core MMA (f16 operands,
+    // fp32 accumulation): scores = q K^T with the block's G query heads as
+    // MMA rows (zero-padded to 16), output += P V.  E4M3 codes convert
+    // straight into f16 operand pairs, one conversion per two elements.
+    // Warp w takes tokens [16w, 16w+16) of each 64-token stage.  Lane
+    // l = 4 gq + c holds query head gq (a real head when gq < G).  A dot
+    // product does not depend on which MMA k position carries which dim, so
+    // lane (gq, c) reads dims [32c, 32c+32) of token 8n + gq of token group n,
+    // and the m-th MMA gets dims 32c+4m+{0,1} at k positions 2c, 2c+1 and
+    // 32c+4m+{2,3} at 2c+8, 2c+9 -- for q and K alike.
+    const int gq = lane >> 2;
+    const int c = lane & 3;
+    // q of head gq as f16 pairs, scaled by the power of two that brings the
+    // row's largest magnitude into [2^14, 2^15): every bf16 element down to
+    // 2^-32 of that maximum converts exactly.  qmul undoes the scaling and
+    // applies the softmax scale (base 2) and the K scale.
+    uint32_t qa[8][2];
+    float qmul;
+    {
+      float qv[32];
+      if (gq < G) {
+        const __nv_bfloat16* qp = p.q + phys_row(qhead(0, gq)) * kHeadDim + 32 * c;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 u = __ldg(reinterpret_cast<const uint4*>(qp) + i);
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            qv[8 * i + 2 * k] = bf16lo(w[k]);
+            qv[8 * i + 2 * k + 1] = bf16hi(w[k]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) qv[i] = 0.f;
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(qv[i]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      // amax = f * 2^e, f in [0.5, 1) (e = -126 for zero and subnormals)
+      const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 126;
+      const int sh = min(15 - e, 100);
+      const float up = __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);
+      qmul = p.scale_log2 * p.k_scale * __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        qa[m][0] = pack_f16x2(qv[4 * m] * up, qv[4 * m + 1] * up);
+        qa[m][1] = pack_f16x2(qv[4 * m + 2] * up, qv[4 * m + 3] * up);
+      }
+    }
+    // output of head gq: MMA n-tile jn, column n is dim 16n + jn, so this
+    // lane's o[jn][0] / o[jn][1] are dims 32c + jn / 32c + 16 + jn
+    // (o[jn][2..3] belong to the zero rows)
+    float o[16][4];
+#pragma unroll
+    for (int jn = 0; jn < 16; ++jn) o[jn][0] = o[jn][1] = o[jn][2] = o[jn][3] = 0.f;
+    float m_run = -INFINITY;  // log2-domain running max of head gq
+    float l_run = 0.f;        // sum of the weights of this lane's tokens
+
+    for (int it = 0; it < n_tiles; ++it) {
+      const int s = it % kStagesN;
+      if (flags[0]) break;
+      if (!mbar_wait(full_bar(s), (it / kStagesN) & 1)) {
+        record_error(p.err, kErrTimeout);
+        flags[0] = 1;
+        break;
+      }
+      const int n_valid = min(kTile, tok_end - (tok_begin + it * kTile));
+      const uint32_t kb = smem_addr(smem + s * kStageB);
+      const uint32_t vb = kb + kOpBytes;
+      const int t0 = 16 * warp;
+
+      // scores of token groups n = 0, 1: row (token) t0 + 8n + gq, whose
+      // 16-byte chunk j sits at chunk j ^ gq (128-byte swizzle)
+      float sc[2][4];
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+        const uint32_t row = kb + (t0 + 8 * n + gq) * 128;
+        const uint4 k0 = lds128(row + (((2 * c) ^ gq) << 4));
+        const uint4 k1 = lds128(row + (((2 * c + 1) ^ gq) << 4));
+        const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+        sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+#pragma unroll
+        for (int mm = 0; mm < 8; ++mm)
+          mma_16x8x16_f16(sc[n], qa[mm][0], 0u, qa[mm][1], 0u, e4m3x2_lo_to_f16x2(kw[mm]),
+                          e4m3x2_hi_to_f16x2(kw[mm]));
+      }
+      // online softmax of head gq over the warp's 16 tokens; this lane has
+      // tokens t0 + 8n + 2c + {0, 1}
+      bool ok[4];
+      float sv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        ok[i] = t0 + 8 * (i >> 1) + 2 * c + (i & 1) < n_valid;
+        sv[i] = ok[i] ? sc[i >> 1][i & 1] * qmul : -INFINITY;
+      }
+      float mt = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+      // the running max moves only when the tile's exceeds it by 2^8
+      if (mt > m_run + 8.f) {
+        const float alpha = rescale(m_run, mt);
+        l_run *= alpha;
+#pragma unroll
+        for (int jn = 0; jn < 16; ++jn) {
+          o[jn][0] *= alpha;
+          o[jn][1] *= alpha;
+        }
+        m_run = mt;
+      }
+      float pw[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) pw[i] = ok[i] ? ex2(sv[i] - m_run) : 0.f;
+      // the weights as the f16 A operand of P V: k positions 2c, 2c+1 are
+      // tokens t0 + 2c, +1 and 2c+8, 2c+9 are t0 + 8 + 2c, +1; the sum takes
+      // the rounded weights the MMA uses
+      const uint32_t pa0 = pack_f16x2(pw[0], pw[1]);
+      const uint32_t pa2 = pack_f16x2(pw[2], pw[3]);
+      l_run += f16x2_sum(pa0) + f16x2_sum(pa2);
+
+      // values: B column gq of n-tile jn is dim 16 gq + jn; this lane gives
+      // k positions 2c, 2c+1 (tokens A, B) and 2c+8, 2c+9 (tokens C, D)
+      uint32_t vw[4][4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int t = t0 + 8 * (k >> 1) + 2 * c + (k & 1);
+        uint4 v = lds128(vb + t * 128 + ((gq ^ (t & 7)) << 4));
+        if (t >= n_valid) v = make_uint4(0u, 0u, 0u, 0u);  // stale slots may hold NaN codes
+        vw[k][0] = v.x;
+        vw[k][1] = v.y;
+        vw[k][2] = v.z;
+        vw[k][3] = v.w;
+      }
+#pragma unroll
+      for (int wi = 0; wi < 4; ++wi) {
+        // bytes 4wi..4wi+3 of two tokens interleaved: pairs for n-tiles 4wi..4wi+3
+        const uint32_t ab01 = __byte_perm(vw[0][wi], vw[1][wi], 0x5140);
+        const uint32_t ab23 = __byte_perm(vw[0][wi], vw[1][wi], 0x7362);
+        const uint32_t cd01 = __byte_perm(vw[2][wi], vw[3][wi], 0x5140);
+        const uint32_t cd23 = __byte_perm(vw[2][wi], vw[3][wi], 0x7362);
+        mma_16x8x16_f16(o[4 * wi], pa0, 0u, pa2, 0u, e4m3x2_lo_to_f16x2(ab01),
+                        e4m3x2_lo_to_f16x2(cd01));
+        mma_16x8x16_f16(o[4 * wi + 1], pa0, 0u, pa2, 0u, e4m3x2_hi_to_f16x2(ab01),
+                        e4m3x2_hi_to_f16x2(cd01));
+        mma_16x8x16_f16(o[4 * wi + 2], pa0, 0u, pa2, 0u, e4m3x2_lo_to_f16x2(ab23),
+                        e4m3x2_lo_to_f16x2(cd23));
+        mma_16x8x16_f16(o[4 * wi + 3], pa0, 0u, pa2, 0u, e4m3x2_hi_to_f16x2(ab23),
+                        e4m3x2_hi_to_f16x2(cd23));
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(empty_bar(s));
+        // refill the stage released one tile ago: by now every warp has
+        // usually released it too, so the issuing lanes seldom wait
+        const int pv = it - 1;
+        if (warp < kIssuers && pv >= 0 && pv + kStagesN < n_tiles && !flags[0]) {
+          if (mbar_wait(empty_bar(pv % kStagesN), (pv / kStagesN) & 1)) {
+            issue(pv + kStagesN);
+          } else {
+            record_error(p.err, kErrTimeout);
+            flags[0] = 1;
+          }
+        }
+      }
+      __syncwarp();
+    }
+
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    if (gq < G) {
+      float* dst = merge_o + (warp * G + gq) * kHeadDim + 32 * c;
+#pragma unroll
+      for (int jn = 0; jn < 16; ++jn) {
+        dst[jn] = o[jn][0];
+        dst[16 + jn] = o[jn][1];
+      }
+      if (c == 0) {
+        merge_m[warp * G + gq] = m_run;
+        merge_l[warp * G + gq] = l_run;
+      }
+    }
+  } else {
     // ------------------------------------------------------------ consumers
     const int grp = lane >> 3;  // group within the warp
     const int j = lane & 7;     // lane within the group: dims [8j,8j+8) and [64+8j,64+8j+8)
@@ -328,17 +513,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     // stage, held in shared-memory row token*KVH + my_hh (128-byte rows).
     // q (pre-scaled into base-2 units) and the running output, as fp32 pairs:
     // pair i < 4 covers dims 8j+2i, 8j+2i+1; pair i >= 4 covers 64+8j+2(i-4), +1.
-    // (FP8: lane j owns dims [16j, 16j+16) instead, pair i = dims 16j+2i, +1,
-    // and q also carries the K scale.)
     f32x2 q2[G][8];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const __nv_bfloat16* qp = p.q + phys_row(qhead(my_hh, h)) * kHeadDim;
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(qp + (kFp8 ? 16 * j : 8 * j)));
-      const uint4 c = __ldg(reinterpret_cast<const uint4*>(qp + (kFp8 ? 16 * j + 8 : 64 + 8 * j)));
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(qp + 8 * j));
+      const uint4 c = __ldg(reinterpret_cast<const uint4*>(qp + 64 + 8 * j));
       const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-      const float qs = kFp8 ? p.scale_log2 * p.k_scale : p.scale_log2;
-      const f32x2 sc2 = pack2(qs, qs);
+      const f32x2 sc2 = pack2(p.scale_log2, p.scale_log2);
 #pragma unroll
       for (int i = 0; i < 8; ++i) q2[h][i] = mul2(bf16x2_to_f32x2(w[i]), sc2);
     }
@@ -374,15 +556,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         const int srow = t * KVH + my_hh;
         const uint32_t off = srow * 128 + ((j ^ (srow & 7)) << 4);
         f32x2 kf[8];
-        if constexpr (kFp8) {
-          const uint4 k0 = lds128(kb + off);
-          const uint32_t w[4] = {k0.x, k0.y, k0.z, k0.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            kf[2 * i] = e4m3x2_to_f32x2(static_cast<uint16_t>(w[i] & 0xFFFFu));
-            kf[2 * i + 1] = e4m3x2_to_f32x2(static_cast<uint16_t>(w[i] >> 16));
-          }
-        } else {
+        {
           const uint4 k0 = lds128(kb + off);
           const uint4 k1 = lds128(kb + kHalfBytes + off);
           const uint32_t w[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
@@ -434,15 +608,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
           const int srow = t * KVH + my_hh;
           const uint32_t off = srow * 128 + ((j ^ (srow & 7)) << 4);
           f32x2 vf[8];
-          if constexpr (kFp8) {
-            const uint4 v0 = lds128(vb + off);
-            const uint32_t w[4] = {v0.x, v0.y, v0.z, v0.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              vf[2 * i] = e4m3x2_to_f32x2(static_cast<uint16_t>(w[i] & 0xFFFFu));
-              vf[2 * i + 1] = e4m3x2_to_f32x2(static_cast<uint16_t>(w[i] >> 16));
-            }
-          } else {
+          {
             const uint4 v0 = lds128(vb + off);
             const uint4 v1 = lds128(vb + kHalfBytes + off);
             const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -460,9 +626,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(empty_bar(s));
-        if (warp < kIssuers && it + kStagesN < n_tiles && !flags[0]) {
-          if (mbar_wait(empty_bar(s), (it / kStagesN) & 1)) {
-            issue(it + kStagesN);
+        // refill the stage released one tile ago: by now every warp has
+        // usually released it too, so the issuing lanes seldom wait
+        const int pv = it - 1;
+        if (warp < kIssuers && pv >= 0 && pv + kStagesN < n_tiles && !flags[0]) {
+          if (mbar_wait(empty_bar(pv % kStagesN), (pv / kStagesN) & 1)) {
+            issue(pv + kStagesN);
           } else {
             record_error(p.err, kErrTimeout);
             flags[0] = 1;
@@ -504,8 +673,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         float* dst = merge_o + (warp * G + h) * kHeadDim;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          dst[(kFp8 ? 16 * j : 8 * j) + i] = o[h][i];
-          dst[(kFp8 ? 16 * j + 8 : 64 + 8 * j) + i] = o[h][8 + i];
+          dst[8 * j + i] = o[h][i];
+          dst[64 + 8 * j + i] = o[h][8 + i];
         }
         if (j == 0) {
           merge_m[warp * G + h] = m[h];

@@ -456,17 +456,54 @@ __device__ __forceinline__ uint16_t e4m3x2_from_f32(float lo, float hi) {
   return r;
 }
 
-// Two E4M3 codes (element 0 in the low byte) -> (element 0, element 1) in
-// fp32; exact (every E4M3 value is an fp16 value).
-__device__ __forceinline__ f32x2 e4m3x2_to_f32x2(uint16_t codes) {
+// The two E4M3 codes in the low (high) 16 bits of w -> an f16x2 pair, the
+// lower-addressed code in the low half; exact (every E4M3 value, subnormals
+// included, is an f16 value).
+__device__ __forceinline__ uint32_t e4m3x2_lo_to_f16x2(uint32_t w) {
   uint32_t h;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(codes));
+  asm("{\n\t.reg .b16 c;\n\tmov.b32 {c, _}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+      : "=r"(h)
+      : "r"(w));
+  return h;
+}
+__device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t w) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 c;\n\tmov.b32 {_, c}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+      : "=r"(h)
+      : "r"(w));
+  return h;
+}
+
+// (lo, hi) -> f16x2, round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// The two halves of an f16x2 pair, summed in fp32.
+__device__ __forceinline__ float f16x2_sum(uint32_t h) {
   float a, b;
   asm("{\n\t.reg .b16 x, y;\n\tmov.b32 {x, y}, %2;\n\tcvt.f32.f16 %0, x;\n\t"
       "cvt.f32.f16 %1, y;\n\t}"
       : "=f"(a), "=f"(b)
       : "r"(h));
-  return pack2(a, b);
+  return a + b;
+}
+
+// ---------------------------------------------------------------- warp-level MMA
+//
+// d += A (16 x 16, f16) * B (16 x 8, f16) with fp32 accumulation, one warp.
+// Lane l = 4 * g + c holds A rows g (a0, a2) and g + 8 (a1, a3) at columns
+// 2c, 2c+1 (a0, a1) and 2c+8, 2c+9 (a2, a3); B column g at rows 2c, 2c+1 (b0)
+// and 2c+8, 2c+9 (b1); d rows g (d0, d1) and g + 8 (d2, d3) at columns 2c, 2c+1.
+__device__ __forceinline__ void mma_16x8x16_f16(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                uint32_t a2, uint32_t a3, uint32_t b0,
+                                                uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 }  // namespace pkv
