@@ -318,67 +318,82 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   if (lane == 0 && warp < kIssuers)
     for (int it = 0; it < kStagesN && it < n_tiles; ++it) issue(it);
 
-  if constexpr (kFp8) {
-    // ---------------------------------------------- consumers, E4M3 pools
-    // Both contractions run on the warp-level tensor-core MMA (f16 operands,
-    // fp32 accumulation): scores = q K^T with the block's G query heads as
-    // MMA rows (zero-padded to 16), output += P V.  E4M3 codes convert
-    // straight into f16 operand pairs, one conversion per two elements.
-    // Warp w takes tokens [16w, 16w+16) of each 64-token stage.  Lane
-    // l = 4 gq + c holds query head gq (a real head when gq < G).  A dot
-    // product does not depend on which MMA k position carries which dim, so
-    // lane (gq, c) reads dims [32c, 32c+32) of token 8n + gq of token group n,
-    // and the m-th MMA gets dims 32c+4m+{0,1} at k positions 2c, 2c+1 and
-    // 32c+4m+{2,3} at 2c+8, 2c+9 -- for q and K alike.
+  {
+    // ------------------------------------------------------------ consumers
+    // Both contractions run on the warp-level tensor-core MMA (16-bit
+    // operands, fp32 accumulation): scores = q K^T with the block's G query
+    // heads as MMA rows, output += P V.  Warp w takes tokens [16w, 16w+16) of
+    // each 64-token stage.  Lane l = 4 gq + c holds row gq (a query head when
+    // gq < G).  A dot product does not depend on which MMA k position carries
+    // which dim, so lane (gq, c) reads dims [32c, 32c+32) of token 8n + gq of
+    // token group n, and the m-th MMA gets dims 32c+4m+{0,1} at k positions
+    // 2c, 2c+1 and 32c+4m+{2,3} at 2c+8, 2c+9, for q and K alike.
+    //   bf16 pools: q and K words are the operands as they are.
+    //   E4M3 pools: each code pair converts to an f16 operand pair (exact);
+    //   q goes to f16 scaled by the power of two that brings its row maximum
+    //   into [2^14, 2^15), where every bf16 element down to 2^-32 of that
+    //   maximum converts exactly.
+    // P V: rows gq carry the weights rounded to 16 bits and rows gq + 8 the
+    // rounded remainders, so the weights enter with about 16 (bf16) or 22
+    // (f16) significant bits.
+    static_assert(KVH == 1, "one kv head per block");
     const int gq = lane >> 2;
     const int c = lane & 3;
-    // q of head gq as f16 pairs, scaled by the power of two that brings the
-    // row's largest magnitude into [2^14, 2^15): every bf16 element down to
-    // 2^-32 of that maximum converts exactly.  qmul undoes the scaling and
-    // applies the softmax scale (base 2) and the K scale.
     uint32_t qa[8][2];
     float qmul;
     {
-      float qv[32];
+      uint32_t qw[16];
       if (gq < G) {
-        const __nv_bfloat16* qp = p.q + phys_row(qhead(0, gq)) * kHeadDim + 32 * c;
+        const uint4* qp = reinterpret_cast<const uint4*>(
+            p.q + phys_row(qhead(0, gq)) * kHeadDim + 32 * c);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const uint4 u = __ldg(reinterpret_cast<const uint4*>(qp) + i);
-          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            qv[8 * i + 2 * k] = bf16lo(w[k]);
-            qv[8 * i + 2 * k + 1] = bf16hi(w[k]);
-          }
+          const uint4 u = __ldg(qp + i);
+          qw[4 * i] = u.x;
+          qw[4 * i + 1] = u.y;
+          qw[4 * i + 2] = u.z;
+          qw[4 * i + 3] = u.w;
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) qv[i] = 0.f;
+        for (int i = 0; i < 16; ++i) qw[i] = 0u;
       }
-      float amax = 0.f;
+      if constexpr (kFp8) {
+        float amax = 0.f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(qv[i]));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      // amax = f * 2^e, f in [0.5, 1) (e = -126 for zero and subnormals)
-      const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 126;
-      const int sh = min(15 - e, 100);
-      const float up = __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);
-      qmul = p.scale_log2 * p.k_scale * __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
+        for (int i = 0; i < 16; ++i)
+          amax = fmaxf(amax, fmaxf(fabsf(bf16lo(qw[i])), fabsf(bf16hi(qw[i]))));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        // amax = f * 2^e, f in [0.5, 1) (e = -126 for zero and subnormals)
+        const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 126;
+        const int sh = min(15 - e, 100);
+        const float up = __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);
+        qmul = p.scale_log2 * p.k_scale *
+               __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        qa[m][0] = pack_f16x2(qv[4 * m] * up, qv[4 * m + 1] * up);
-        qa[m][1] = pack_f16x2(qv[4 * m + 2] * up, qv[4 * m + 3] * up);
+        for (int m = 0; m < 8; ++m) {
+          qa[m][0] = pack_f16x2(bf16lo(qw[2 * m]) * up, bf16hi(qw[2 * m]) * up);
+          qa[m][1] = pack_f16x2(bf16lo(qw[2 * m + 1]) * up, bf16hi(qw[2 * m + 1]) * up);
+        }
+      } else {
+        qmul = p.scale_log2;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          qa[m][0] = qw[2 * m];
+          qa[m][1] = qw[2 * m + 1];
+        }
       }
     }
-    // output of head gq: MMA n-tile jn, column n is dim 16n + jn, so this
-    // lane's o[jn][0] / o[jn][1] are dims 32c + jn / 32c + 16 + jn
-    // (o[jn][2..3] belong to the zero rows)
+    // keys of this split row gq may see (several query positions only)
+    const int lim = kMQ ? key_limit(qhead(0, gq < G ? gq : 0)) - tok_begin : 0;
+    // o[jn][0..1]: rows gq, o[jn][2..3]: rows gq + 8 (the weight remainders);
+    // summed when the loop ends.  Output column n of n-tile jn is dim
+    // vdim(n, jn) below.
     float o[16][4];
 #pragma unroll
     for (int jn = 0; jn < 16; ++jn) o[jn][0] = o[jn][1] = o[jn][2] = o[jn][3] = 0.f;
-    float m_run = -INFINITY;  // log2-domain running max of head gq
+    float m_run = -INFINITY;  // log2-domain running max of row gq
     float l_run = 0.f;        // sum of the weights of this lane's tokens
 
     for (int it = 0; it < n_tiles; ++it) {
@@ -394,34 +409,54 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       const uint32_t vb = kb + kOpBytes;
       const int t0 = 16 * warp;
 
-      // scores of token groups n = 0, 1: row (token) t0 + 8n + gq, whose
-      // 16-byte chunk j sits at chunk j ^ gq (128-byte swizzle)
+      // scores of token groups n = 0, 1: row (token) t0 + 8n + gq; a
+      // 128-byte row's 16-byte chunk j sits at chunk j ^ (row & 7) = j ^ gq
       float sc[2][4];
 #pragma unroll
       for (int n = 0; n < 2; ++n) {
-        const uint32_t row = kb + (t0 + 8 * n + gq) * 128;
-        const uint4 k0 = lds128(row + (((2 * c) ^ gq) << 4));
-        const uint4 k1 = lds128(row + (((2 * c + 1) ^ gq) << 4));
-        const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+        uint32_t kw[16];
+        if constexpr (kFp8) {
+          const uint32_t row = kb + (t0 + 8 * n + gq) * 128;
+          const uint4 k0 = lds128(row + (((2 * c) ^ gq) << 4));
+          const uint4 k1 = lds128(row + (((2 * c + 1) ^ gq) << 4));
+          const uint32_t w[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            kw[2 * i] = e4m3x2_lo_to_f16x2(w[i]);
+            kw[2 * i + 1] = e4m3x2_hi_to_f16x2(w[i]);
+          }
+        } else {
+          // dims [32c, 32c+32): half c >> 1, chunks 4 (c & 1) .. + 3
+          const uint32_t row = kb + (c >> 1) * kHalfBytes + (t0 + 8 * n + gq) * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 u = lds128(row + (((4 * (c & 1) + i) ^ gq) << 4));
+            kw[4 * i] = u.x;
+            kw[4 * i + 1] = u.y;
+            kw[4 * i + 2] = u.z;
+            kw[4 * i + 3] = u.w;
+          }
+        }
         sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
 #pragma unroll
         for (int mm = 0; mm < 8; ++mm)
-          mma_16x8x16_f16(sc[n], qa[mm][0], 0u, qa[mm][1], 0u, e4m3x2_lo_to_f16x2(kw[mm]),
-                          e4m3x2_hi_to_f16x2(kw[mm]));
+          mma_16x8x16<kFp8>(sc[n], qa[mm][0], 0u, qa[mm][1], 0u, kw[2 * mm], kw[2 * mm + 1]);
       }
-      // online softmax of head gq over the warp's 16 tokens; this lane has
-      // tokens t0 + 8n + 2c + {0, 1}
+      // online softmax of row gq over the warp's 16 tokens; this lane has
+      // tokens t0 + 8 (i >> 1) + 2c + (i & 1), i = 0..3
       bool ok[4];
       float sv[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        ok[i] = t0 + 8 * (i >> 1) + 2 * c + (i & 1) < n_valid;
+        const int t = t0 + 8 * (i >> 1) + 2 * c + (i & 1);
+        ok[i] = t < n_valid && (!kMQ || it * kTile + t < lim);
         sv[i] = ok[i] ? sc[i >> 1][i & 1] * qmul : -INFINITY;
       }
       float mt = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
       mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
       mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-      // the running max moves only when the tile's exceeds it by 2^8
+      // the running max moves only when the tile's exceeds it by 2^8; below
+      // that the weights stay within 256 and o is not rescaled
       if (mt > m_run + 8.f) {
         const float alpha = rescale(m_run, mt);
         l_run *= alpha;
@@ -429,47 +464,85 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         for (int jn = 0; jn < 16; ++jn) {
           o[jn][0] *= alpha;
           o[jn][1] *= alpha;
+          o[jn][2] *= alpha;
+          o[jn][3] *= alpha;
         }
         m_run = mt;
       }
       float pw[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) pw[i] = ok[i] ? ex2(sv[i] - m_run) : 0.f;
-      // the weights as the f16 A operand of P V: k positions 2c, 2c+1 are
-      // tokens t0 + 2c, +1 and 2c+8, 2c+9 are t0 + 8 + 2c, +1; the sum takes
-      // the rounded weights the MMA uses
-      const uint32_t pa0 = pack_f16x2(pw[0], pw[1]);
-      const uint32_t pa2 = pack_f16x2(pw[2], pw[3]);
-      l_run += f16x2_sum(pa0) + f16x2_sum(pa2);
-
-      // values: B column gq of n-tile jn is dim 16 gq + jn; this lane gives
-      // k positions 2c, 2c+1 (tokens A, B) and 2c+8, 2c+9 (tokens C, D)
-      uint32_t vw[4][4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int t = t0 + 8 * (k >> 1) + 2 * c + (k & 1);
-        uint4 v = lds128(vb + t * 128 + ((gq ^ (t & 7)) << 4));
-        if (t >= n_valid) v = make_uint4(0u, 0u, 0u, 0u);  // stale slots may hold NaN codes
-        vw[k][0] = v.x;
-        vw[k][1] = v.y;
-        vw[k][2] = v.z;
-        vw[k][3] = v.w;
+      for (int i = 0; i < 4; ++i) {
+        pw[i] = ok[i] ? ex2(sv[i] - m_run) : 0.f;
+        l_run += pw[i];
       }
+      // A operand of P V: k positions 2c, 2c+1 are tokens t0 + 2c, +1 (a0 / a1)
+      // and 2c+8, 2c+9 tokens t0 + 8 + 2c, +1 (a2 / a3)
+      uint32_t ph0, pl0, ph2, pl2;
+      split_pair<kFp8>(pw[0], pw[1], ph0, pl0);
+      split_pair<kFp8>(pw[2], pw[3], ph2, pl2);
+
+      // values: this lane gives B column gq at k positions 2c, 2c+1 (tokens
+      // A, B) and 2c+8, 2c+9 (tokens C, D).  Tokens past the context are
+      // zeroed: stale slots may hold NaN patterns.
+      if constexpr (kFp8) {
+        // column gq of n-tile jn is dim 16 gq + jn: byte jn of the chunk
+        uint32_t vw[4][4];
 #pragma unroll
-      for (int wi = 0; wi < 4; ++wi) {
-        // bytes 4wi..4wi+3 of two tokens interleaved: pairs for n-tiles 4wi..4wi+3
-        const uint32_t ab01 = __byte_perm(vw[0][wi], vw[1][wi], 0x5140);
-        const uint32_t ab23 = __byte_perm(vw[0][wi], vw[1][wi], 0x7362);
-        const uint32_t cd01 = __byte_perm(vw[2][wi], vw[3][wi], 0x5140);
-        const uint32_t cd23 = __byte_perm(vw[2][wi], vw[3][wi], 0x7362);
-        mma_16x8x16_f16(o[4 * wi], pa0, 0u, pa2, 0u, e4m3x2_lo_to_f16x2(ab01),
-                        e4m3x2_lo_to_f16x2(cd01));
-        mma_16x8x16_f16(o[4 * wi + 1], pa0, 0u, pa2, 0u, e4m3x2_hi_to_f16x2(ab01),
-                        e4m3x2_hi_to_f16x2(cd01));
-        mma_16x8x16_f16(o[4 * wi + 2], pa0, 0u, pa2, 0u, e4m3x2_lo_to_f16x2(ab23),
-                        e4m3x2_lo_to_f16x2(cd23));
-        mma_16x8x16_f16(o[4 * wi + 3], pa0, 0u, pa2, 0u, e4m3x2_hi_to_f16x2(ab23),
-                        e4m3x2_hi_to_f16x2(cd23));
+        for (int k = 0; k < 4; ++k) {
+          const int t = t0 + 8 * (k >> 1) + 2 * c + (k & 1);
+          uint4 v = lds128(vb + t * 128 + ((gq ^ (t & 7)) << 4));
+          if (t >= n_valid) v = make_uint4(0u, 0u, 0u, 0u);
+          vw[k][0] = v.x;
+          vw[k][1] = v.y;
+          vw[k][2] = v.z;
+          vw[k][3] = v.w;
+        }
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+          // bytes 4wi..4wi+3 of two tokens interleaved: n-tiles 4wi..4wi+3
+          const uint32_t ab01 = __byte_perm(vw[0][wi], vw[1][wi], 0x5140);
+          const uint32_t ab23 = __byte_perm(vw[0][wi], vw[1][wi], 0x7362);
+          const uint32_t cd01 = __byte_perm(vw[2][wi], vw[3][wi], 0x5140);
+          const uint32_t cd23 = __byte_perm(vw[2][wi], vw[3][wi], 0x7362);
+          mma_16x8x16<true>(o[4 * wi], ph0, pl0, ph2, pl2, e4m3x2_lo_to_f16x2(ab01),
+                            e4m3x2_lo_to_f16x2(cd01));
+          mma_16x8x16<true>(o[4 * wi + 1], ph0, pl0, ph2, pl2, e4m3x2_hi_to_f16x2(ab01),
+                            e4m3x2_hi_to_f16x2(cd01));
+          mma_16x8x16<true>(o[4 * wi + 2], ph0, pl0, ph2, pl2, e4m3x2_lo_to_f16x2(ab23),
+                            e4m3x2_lo_to_f16x2(cd23));
+          mma_16x8x16<true>(o[4 * wi + 3], ph0, pl0, ph2, pl2, e4m3x2_hi_to_f16x2(ab23),
+                            e4m3x2_hi_to_f16x2(cd23));
+        }
+      } else {
+        // dims [16 gq, 16 gq + 16): half gq >> 2, chunks 2 (gq & 3) + {0, 1},
+        // the two loaded in the order (gq & 1, 1 - (gq & 1)) so that each load
+        // instruction touches all eight chunk positions; load i then holds
+        // dims 16 gq + 8 (i ^ (gq & 1)) + 0..7, and column gq of n-tile jn is
+        // dim 16 gq + (jn ^ 8 (gq & 1))
+        uint32_t vw[4][8];
+        const uint32_t vhalf = vb + (gq >> 2) * kHalfBytes;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int t = t0 + 8 * (k >> 1) + 2 * c + (k & 1);
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int chunk = 2 * (gq & 3) + (i ^ (gq & 1));
+            uint4 v = lds128(vhalf + t * 128 + ((chunk ^ (t & 7)) << 4));
+            if (t >= n_valid) v = make_uint4(0u, 0u, 0u, 0u);
+            vw[k][4 * i] = v.x;
+            vw[k][4 * i + 1] = v.y;
+            vw[k][4 * i + 2] = v.z;
+            vw[k][4 * i + 3] = v.w;
+          }
+        }
+#pragma unroll
+        for (int jn = 0; jn < 16; ++jn) {
+          // word jn >> 1 holds the dims 2 (jn >> 1), +1 of load jn >> 3
+          const uint32_t sel = (jn & 1) ? 0x7632u : 0x5410u;
+          const uint32_t b0 = __byte_perm(vw[0][jn >> 1], vw[1][jn >> 1], sel);
+          const uint32_t b1 = __byte_perm(vw[2][jn >> 1], vw[3][jn >> 1], sel);
+          mma_16x8x16<false>(o[jn], ph0, pl0, ph2, pl2, b0, b1);
+        }
       }
       __syncwarp();
       if (lane == 0) {
@@ -492,194 +565,17 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
     if (gq < G) {
+      // this lane's output columns: n = 2c at dims 32c + jn and n = 2c + 1 at
+      // dims 32c + 16 + jn (bf16: 32c + 16 + (jn ^ 8))
       float* dst = merge_o + (warp * G + gq) * kHeadDim + 32 * c;
 #pragma unroll
       for (int jn = 0; jn < 16; ++jn) {
-        dst[jn] = o[jn][0];
-        dst[16 + jn] = o[jn][1];
+        dst[jn] = o[jn][0] + o[jn][2];
+        dst[16 + (kFp8 ? jn : (jn ^ 8))] = o[jn][1] + o[jn][3];
       }
       if (c == 0) {
         merge_m[warp * G + gq] = m_run;
         merge_l[warp * G + gq] = l_run;
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ consumers
-    const int grp = lane >> 3;  // group within the warp
-    const int j = lane & 7;     // lane within the group: dims [8j,8j+8) and [64+8j,64+8j+8)
-    const int my_hh = warp / kWPH;   // this warp's kv head within the block
-    const int my_wl = warp % kWPH;   // this warp's index among that head's warps
-    // Tile row r (0..3) of this group is token 4*(r*kWPH + my_wl) + grp of the
-    // stage, held in shared-memory row token*KVH + my_hh (128-byte rows).
-    // q (pre-scaled into base-2 units) and the running output, as fp32 pairs:
-    // pair i < 4 covers dims 8j+2i, 8j+2i+1; pair i >= 4 covers 64+8j+2(i-4), +1.
-    f32x2 q2[G][8];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const __nv_bfloat16* qp = p.q + phys_row(qhead(my_hh, h)) * kHeadDim;
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(qp + 8 * j));
-      const uint4 c = __ldg(reinterpret_cast<const uint4*>(qp + 64 + 8 * j));
-      const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-      const f32x2 sc2 = pack2(p.scale_log2, p.scale_log2);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) q2[h][i] = mul2(bf16x2_to_f32x2(w[i]), sc2);
-    }
-    f32x2 o2[G][8];
-    float m[G], l[G];
-    int lim[G];   // keys of this split visible to head h: tile-relative index < lim
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      m[h] = -INFINITY;
-      l[h] = 0.f;
-      lim[h] = kMQ ? key_limit(qhead(my_hh, h)) - tok_begin : 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) o2[h][i] = 0ull;
-    }
-
-    for (int it = 0; it < n_tiles; ++it) {
-      const int s = it % kStagesN;
-      if (flags[0]) break;
-      if (!mbar_wait(full_bar(s), (it / kStagesN) & 1)) {
-        record_error(p.err, kErrTimeout);
-        flags[0] = 1;
-        break;
-      }
-      const int n_valid = min(kTT, tok_end - (tok_begin + it * kTT));
-      const uint32_t kb = smem_addr(smem + s * kStageB);
-      const uint32_t vb = kb + kOpBytes;
-
-      // scores of this group's four rows of the tile, base-2 units
-      float sc[4][G];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int t = 4 * (r * kWPH + my_wl) + grp;
-        const int srow = t * KVH + my_hh;
-        const uint32_t off = srow * 128 + ((j ^ (srow & 7)) << 4);
-        f32x2 kf[8];
-        {
-          const uint4 k0 = lds128(kb + off);
-          const uint4 k1 = lds128(kb + kHalfBytes + off);
-          const uint32_t w[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) kf[i] = bf16x2_to_f32x2(w[i]);
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          f32x2 a0 = mul2(q2[h][0], kf[0]);
-          f32x2 a1 = mul2(q2[h][1], kf[1]);
-#pragma unroll
-          for (int i = 2; i < 8; i += 2) {
-            a0 = fma2(q2[h][i], kf[i], a0);
-            a1 = fma2(q2[h][i + 1], kf[i + 1], a1);
-          }
-          a0 = add2(a0, a1);
-          float acc = lo2(a0) + hi2(a0);
-          acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-          acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-          acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-          sc[r][h] = (t < n_valid && (!kMQ || it * kTT + t < lim[h])) ? acc : -INFINITY;
-        }
-      }
-      // online softmax, once per tile.  The running max only moves when the
-      // tile's max exceeds it by more than 2^8; below that the stale max is
-      // kept (weights up to 256 are exact enough in fp32) and o is not rescaled.
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float mt = fmaxf(fmaxf(sc[0][h], sc[1][h]), fmaxf(sc[2][h], sc[3][h]));
-        if (mt > m[h] + 8.f) {
-          const float alpha = rescale(m[h], mt);
-          l[h] *= alpha;
-          const f32x2 a2 = pack2(alpha, alpha);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) o2[h][i] = mul2(o2[h][i], a2);
-          m[h] = mt;
-        }
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int t = 4 * (r * kWPH + my_wl) + grp;
-          sc[r][h] = (t < n_valid && (!kMQ || it * kTT + t < lim[h])) ? ex2(sc[r][h] - m[h]) : 0.f;
-          l[h] += sc[r][h];
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int t = 4 * (r * kWPH + my_wl) + grp;
-        if (t < n_valid) {
-          const int srow = t * KVH + my_hh;
-          const uint32_t off = srow * 128 + ((j ^ (srow & 7)) << 4);
-          f32x2 vf[8];
-          {
-            const uint4 v0 = lds128(vb + off);
-            const uint4 v1 = lds128(vb + kHalfBytes + off);
-            const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) vf[i] = bf16x2_to_f32x2(w[i]);
-          }
-#pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const f32x2 p2 = pack2(sc[r][h], sc[r][h]);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) o2[h][i] = fma2(p2, vf[i], o2[h][i]);
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(empty_bar(s));
-        // refill the stage released one tile ago: by now every warp has
-        // usually released it too, so the issuing lanes seldom wait
-        const int pv = it - 1;
-        if (warp < kIssuers && pv >= 0 && pv + kStagesN < n_tiles && !flags[0]) {
-          if (mbar_wait(empty_bar(pv % kStagesN), (pv / kStagesN) & 1)) {
-            issue(pv + kStagesN);
-          } else {
-            record_error(p.err, kErrTimeout);
-            flags[0] = 1;
-          }
-        }
-      }
-      __syncwarp();
-    }
-
-    float o[G][16];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        o[h][2 * i] = lo2(o2[h][i]);
-        o[h][2 * i + 1] = hi2(o2[h][i]);
-      }
-    }
-
-    // merge the four groups of this warp (lanes j, j+8, j+16, j+24)
-#pragma unroll
-    for (int sh = 8; sh <= 16; sh <<= 1) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float mo = __shfl_xor_sync(0xffffffffu, m[h], sh);
-        const float lo = __shfl_xor_sync(0xffffffffu, l[h], sh);
-        const float mn = fmaxf(m[h], mo);
-        const float a = rescale(m[h], mn), c = rescale(mo, mn);
-        l[h] = l[h] * a + lo * c;
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          o[h][i] = o[h][i] * a + __shfl_xor_sync(0xffffffffu, o[h][i], sh) * c;
-        m[h] = mn;
-      }
-    }
-    if (grp == 0) {
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float* dst = merge_o + (warp * G + h) * kHeadDim;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          dst[8 * j + i] = o[h][i];
-          dst[64 + 8 * j + i] = o[h][8 + i];
-        }
-        if (j == 0) {
-          merge_m[warp * G + h] = m[h];
-          merge_l[warp * G + h] = l[h];
-        }
       }
     }
   }

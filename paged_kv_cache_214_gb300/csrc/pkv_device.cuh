@@ -481,29 +481,52 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return r;
 }
 
-// The two halves of an f16x2 pair, summed in fp32.
-__device__ __forceinline__ float f16x2_sum(uint32_t h) {
-  float a, b;
+// An f16x2 pair -> (lo, hi) in fp32 (exact).
+__device__ __forceinline__ void f16x2_unpack(uint32_t h, float& lo, float& hi) {
   asm("{\n\t.reg .b16 x, y;\n\tmov.b32 {x, y}, %2;\n\tcvt.f32.f16 %0, x;\n\t"
       "cvt.f32.f16 %1, y;\n\t}"
-      : "=f"(a), "=f"(b)
+      : "=f"(lo), "=f"(hi)
       : "r"(h));
-  return a + b;
+}
+
+// (a, b) as the sum of two 16-bit pairs, hi + lo: hi is (a, b) rounded, lo
+// the rounded remainder, so that hi + lo carries about twice the precision of
+// one 16-bit value.  f16 for kF16, else bf16.
+template <bool kF16>
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
+  float ah, bh;
+  if constexpr (kF16) {
+    hi = pack_f16x2(a, b);
+    f16x2_unpack(hi, ah, bh);
+    lo = pack_f16x2(a - ah, b - bh);
+  } else {
+    hi = pack_bf16x2(a, b);
+    ah = bf16lo(hi);
+    bh = bf16hi(hi);
+    lo = pack_bf16x2(a - ah, b - bh);
+  }
 }
 
 // ---------------------------------------------------------------- warp-level MMA
 //
-// d += A (16 x 16, f16) * B (16 x 8, f16) with fp32 accumulation, one warp.
+// d += A (16 x 16) * B (16 x 8), 16-bit operands, fp32 accumulation, one warp.
 // Lane l = 4 * g + c holds A rows g (a0, a2) and g + 8 (a1, a3) at columns
 // 2c, 2c+1 (a0, a1) and 2c+8, 2c+9 (a2, a3); B column g at rows 2c, 2c+1 (b0)
 // and 2c+8, 2c+9 (b1); d rows g (d0, d1) and g + 8 (d2, d3) at columns 2c, 2c+1.
-__device__ __forceinline__ void mma_16x8x16_f16(float (&d)[4], uint32_t a0, uint32_t a1,
-                                                uint32_t a2, uint32_t a3, uint32_t b0,
-                                                uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
-      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+// kF16: f16 operands, else bf16.
+template <bool kF16>
+__device__ __forceinline__ void mma_16x8x16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                            uint32_t a3, uint32_t b0, uint32_t b1) {
+  if constexpr (kF16)
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  else
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 }  // namespace pkv
