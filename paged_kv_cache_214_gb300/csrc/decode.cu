@@ -12,27 +12,29 @@
 //   (sequence, kv head, range of whole KV blocks) and serves the G query heads
 //   of that kv head's group that it is assigned, so each K/V byte is read from
 //   HBM once per G heads.
-//   The range's K and V stream through a 3-stage ring of shared-memory tiles
-//   with TMA (64 tokens x 128 dims per tile; two 64-dim boxes per operand,
-//   128-byte swizzle) and mbarrier completion; lane 0 of warp 0 issues the
-//   copies, refilling a stage as soon as all four warps have released it.
-//   Four warps (two blocks per SM, so up to 255 registers a thread): sixteen
-//   8-lane groups, each an independent online
-//   softmax stream.  Lane j of a group owns dims [8j, 8j+8) and [64+8j, 64+8j+8)
-//   of q and of the running output for all G heads, all in registers.  A group
-//   takes one token row per step: 16 partial products per head (8 packed
-//   fp32x2 FMAs), a 3-level butterfly to finish the dot product, then, once
-//   per tile, the running max / sum update and o += p * v on the same 16 dims
-//   (8 packed FMAs per head).
-//   End of the range: the 16 streams are merged by log-sum-exp (shuffles
-//   across the groups of a warp, then shared memory across warps).
-//   With one split the block writes out/lse directly.  Otherwise it writes a
-//   normalised partial (o, log2-sum-exp) to the workspace and takes a ticket
-//   from the (sequence, head group) counter; the last block to arrive merges all
-//   partials with a warp-shuffle log-sum-exp reduction, writes out/lse and
-//   resets the counter, so nothing ever spins.
-// Scores are kept in base-2 units (q is pre-scaled by scale*log2(e)) and
-// converted to a natural-log LSE on output.
+//   The range's K and V stream through a ring of shared-memory stages with
+//   TMA (64 tokens x 128 dims per stage, 128-byte swizzle) and mbarrier
+//   completion: bf16 pools 3 stages, each operand two 64-dim boxes; E4M3
+//   pools (one byte per element) 4 stages of one 128-byte box per operand.
+//   Lane 0 of the issuing warps copies one box each and refills the stage
+//   released one tile earlier.
+//   Four warps consume, warp w taking tokens [16w, 16w+16) of every stage.
+//   Both contractions run on the warp-level tensor-core MMA (m16n8k16,
+//   16-bit operands, fp32 accumulation) with the G query heads as MMA rows:
+//   scores = q K^T straight from the stage (bf16 words as they are; E4M3
+//   pairs converted to f16 pairs, exactly), an online softmax per row, then
+//   o += P V with V pairs formed by byte permutes.  The MMA rows past the
+//   heads carry the rounded remainder of the weights, so P enters with about
+//   16 (bf16) or 22 (f16) significant bits.
+//   End of the range: the four warps' streams are merged by log-sum-exp
+//   through shared memory.  With one split the block writes out/lse
+//   directly.  Otherwise it writes a normalised partial (o, log2-sum-exp) to
+//   the workspace and takes a ticket from the (sequence, head group)
+//   counter; the last block to arrive merges all partials with a
+//   warp-shuffle log-sum-exp reduction, writes out/lse and resets the
+//   counter, so nothing ever spins.
+// Scores are kept in base-2 units (the score multiplier includes log2(e))
+// and converted to a natural-log LSE on output.
 
 #include <cuda_bf16.h>
 #include <math.h>
@@ -91,7 +93,8 @@ struct DecodeParams {
 // Log-sum-exp merge of one output row by one warp: nsplit partials
 // (lse2[s], o[s][128]) of the row's own tokens plus np partials of a shared
 // prefix, all normalised.  Lanes run over partials for the max and the sum
-// (warp shuffles), then over dims (4 each) for the weighted sum.
+// (warp shuffles), then over dims (4 each) for the weighted sum, eight
+// partials at a time so that their loads are in flight together.
 __device__ __forceinline__ void merge_row(const float* lrow, const float* orow, int nsplit,
                                           const float* plrow, const float* porow, int np,
                                           __nv_bfloat16* out, float* lse, int lane) {
@@ -107,16 +110,31 @@ __device__ __forceinline__ void merge_row(const float* lrow, const float* orow, 
   for (int sh = 16; sh >= 1; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
   const float inv = 1.f / sum;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  auto add = [&](const float* o, float l2) {
-    const float w = ex2(l2 - mx) * inv;
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(o) + lane);
-    acc.x = fmaf(w, v.x, acc.x);
-    acc.y = fmaf(w, v.y, acc.y);
-    acc.z = fmaf(w, v.z, acc.z);
-    acc.w = fmaf(w, v.w, acc.w);
+  auto add = [&](const float* lr, const float* orr, int n) {
+    for (int s0 = 0; s0 < n; s0 += 8) {
+      float l8[8];
+      float4 v8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (s0 + k < n) {
+          l8[k] = __ldcg(lr + s0 + k);
+          v8[k] = __ldcg(reinterpret_cast<const float4*>(orr + (s0 + k) * kHeadDim) + lane);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (s0 + k < n) {
+          const float w = ex2(l8[k] - mx) * inv;
+          acc.x = fmaf(w, v8[k].x, acc.x);
+          acc.y = fmaf(w, v8[k].y, acc.y);
+          acc.z = fmaf(w, v8[k].z, acc.z);
+          acc.w = fmaf(w, v8[k].w, acc.w);
+        }
+      }
+    }
   };
-  for (int s = 0; s < np; ++s) add(porow + s * kHeadDim, __ldcg(plrow + s));
-  for (int s = 0; s < nsplit; ++s) add(orow + s * kHeadDim, __ldcg(lrow + s));
+  add(plrow, porow, np);
+  add(lrow, orow, nsplit);
   __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y);
   __nv_bfloat162 hi2 = __floats2bfloat162_rn(acc.z, acc.w);
   uint2 packed;
@@ -161,12 +179,12 @@ __device__ __forceinline__ float rescale(float m, float mn) {
 }
 
 // kMQ: several query positions per sequence (q_len > 1); plain decode
-// compiles without the per-row key limits.  kFp8: E4M3 pools (KVH = 1 only).
-template <int G, int KVH, bool kMQ, bool kFp8>
+// compiles without the per-row key limits.  kFp8: E4M3 pools.  One kv head
+// per block; G of its query heads.
+template <int G, bool kMQ, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 2)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
-  static_assert(!kFp8 || KVH == 1, "FP8 pools are read one kv head per block");
   using L = SmemLayout<G, kFp8>;
   constexpr int kStagesN = Geo<kFp8>::kStagesN;
   constexpr int kStageB = Geo<kFp8>::kStageB;
@@ -184,18 +202,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (kStagesN + s); };
 
-  // KVH kv heads per block: each pipeline stage holds kTT tokens x KVH heads
-  // (so a token contributes one contiguous KVH x 256-byte chunk), and
-  // kWPH = 4 / KVH warps work on each of the block's kv heads.
-  constexpr int kTT = kTile / KVH;
-  constexpr int kWPH = kConsumerWarps / KVH;
   const int split = blockIdx.x;
-  const int hg = blockIdx.y;  // (kv head group of KVH) * head_groups + query head group
+  const int hg = blockIdx.y;  // kv head * head_groups + query head group
   const int b = blockIdx.z;
   const int g = p.Hq / p.Hkv;
-  const int kvh0 = (hg / p.head_groups) * KVH;   // first kv head of the block
-  const int hoff = (hg % p.head_groups) * G;     // first query head within each group
-  auto qhead = [&](int hh, int h) { return (kvh0 + hh) * g + hoff + h; };
+  const int kvh0 = hg / p.head_groups;           // the block's kv head
+  const int hoff = (hg % p.head_groups) * G;     // first query head within its group
+  auto qhead = [&](int h) { return kvh0 * g + hoff + h; };
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -242,26 +255,26 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 
   if (ctx == P) {  // nothing past the prefix: out = the prefix's result (or 0, -inf)
     if (P > 0) {
-      for (int r = warp; r < KVH * G; r += kConsumerWarps) {
-        const int64_t row = static_cast<int64_t>(b) * p.Hq + qhead(r / G, r % G);
+      for (int r = warp; r < G; r += kConsumerWarps) {
+        const int64_t row = static_cast<int64_t>(b) * p.Hq + qhead(r);
         const int np = p.prefix_splits;
-        const int64_t prow = phys_row(qhead(r / G, r % G));
+        const int64_t prow = phys_row(qhead(r));
         merge_row(nullptr, nullptr, 0, p.prefix_lse + row * np, p.prefix_o + row * np * kHeadDim,
                   np, p.out + prow * kHeadDim, p.lse ? p.lse + prow : nullptr, lane);
       }
       return;
     }
-    for (int i = tid; i < KVH * G * kHeadDim; i += kThreads) {
+    for (int i = tid; i < G * kHeadDim; i += kThreads) {
       const int r = i / kHeadDim, d = i % kHeadDim;
-      p.out[phys_row(qhead(r / G, r % G)) * kHeadDim + d] = __float2bfloat16_rn(0.f);
+      p.out[phys_row(qhead(r)) * kHeadDim + d] = __float2bfloat16_rn(0.f);
     }
-    if (p.lse && tid < KVH * G) p.lse[phys_row(qhead(tid / G, tid % G))] = -INFINITY;
+    if (p.lse && tid < G) p.lse[phys_row(qhead(tid))] = -INFINITY;
     return;
   }
 
   const int tok_begin = P + split * split_tokens;
   const int tok_end = min(ctx, tok_begin + split_tokens);
-  const int n_tiles = (tok_end - tok_begin + kTT - 1) / kTT;
+  const int n_tiles = (tok_end - tok_begin + kTile - 1) / kTile;
 
   // Every warp is a producer for one quarter of each stage (warp w loads
   // K dims [0,64), K [64,128), V [0,64), V [64,128) for w = 0..3): one thread
@@ -272,7 +285,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   const uint64_t policy = l2_policy_evict_first();
   auto issue = [&](int it) {
     const int s = it % kStagesN;
-    const int tok = tok_begin + it * kTT;
+    const int tok = tok_begin + it * kTile;
     const int slot = sblk[tok / kBlockSize - blk_begin] * kBlockSize + tok % kBlockSize;
     if constexpr (kFp8) {
       // warp 0: the K tile, warp 1: the V tile (one 128-byte-wide box each)
@@ -336,7 +349,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     // P V: rows gq carry the weights rounded to 16 bits and rows gq + 8 the
     // rounded remainders, so the weights enter with about 16 (bf16) or 22
     // (f16) significant bits.
-    static_assert(KVH == 1, "one kv head per block");
     const int gq = lane >> 2;
     const int c = lane & 3;
     uint32_t qa[8][2];
@@ -345,7 +357,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       uint32_t qw[16];
       if (gq < G) {
         const uint4* qp = reinterpret_cast<const uint4*>(
-            p.q + phys_row(qhead(0, gq)) * kHeadDim + 32 * c);
+            p.q + phys_row(qhead(gq)) * kHeadDim + 32 * c);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const uint4 u = __ldg(qp + i);
@@ -386,7 +398,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       }
     }
     // keys of this split row gq may see (several query positions only)
-    const int lim = kMQ ? key_limit(qhead(0, gq < G ? gq : 0)) - tok_begin : 0;
+    const int lim = kMQ ? key_limit(qhead(gq < G ? gq : 0)) - tok_begin : 0;
     // o[jn][0..1]: rows gq, o[jn][2..3]: rows gq + 8 (the weight remainders);
     // summed when the loop ends.  Output column n of n-tile jn is dim
     // vdim(n, jn) below.
@@ -596,14 +608,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   // thread tid (0..127) owns dim d = tid of every head
   const int d = tid;
   const bool single = nsplit == 1 && P == 0;
-  for (int r = 0; r < KVH * G; ++r) {
-    const int hh = r / G, h = r % G;
+  for (int h = 0; h < G; ++h) {
     float M = -INFINITY;
 #pragma unroll
-    for (int w = hh * kWPH; w < (hh + 1) * kWPH; ++w) M = fmaxf(M, merge_m[w * G + h]);
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge_m[w * G + h]);
     float Ls = 0.f, Os = 0.f;
 #pragma unroll
-    for (int w = hh * kWPH; w < (hh + 1) * kWPH; ++w) {
+    for (int w = 0; w < kConsumerWarps; ++w) {
       const float c = rescale(merge_m[w * G + h], M);
       Ls += merge_l[w * G + h] * c;
       Os += merge_o[(w * G + h) * kHeadDim + d] * c;
@@ -613,9 +624,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     float on = Ls > 0.f ? Os / Ls : 0.f;
     if constexpr (kFp8) on *= p.v_scale;
     const float lse2 = M + __log2f(Ls);
-    const int64_t row = static_cast<int64_t>(b) * p.Hq + qhead(hh, h);
+    const int64_t row = static_cast<int64_t>(b) * p.Hq + qhead(h);
     if (single) {
-      const int64_t orow = phys_row(qhead(hh, h));
+      const int64_t orow = phys_row(qhead(h));
       p.out[orow * kHeadDim + d] = __float2bfloat16_rn(on);
       if (p.lse && d == 0) p.lse[orow] = lse2 * kLn2;
     } else {
@@ -640,9 +651,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   }
   named_barrier(1, kConsumerWarps * 32);
   if (!flags[1]) return;
-  for (int r = warp; r < KVH * G; r += kConsumerWarps) {
-    const int64_t row = static_cast<int64_t>(b) * p.Hq + qhead(r / G, r % G);
-    const int64_t orow = phys_row(qhead(r / G, r % G));
+  for (int r = warp; r < G; r += kConsumerWarps) {
+    const int64_t row = static_cast<int64_t>(b) * p.Hq + qhead(r);
+    const int64_t orow = phys_row(qhead(r));
     const int np = P > 0 ? p.prefix_splits : 0;
     merge_row(p.ws_lse + row * p.num_splits, p.ws_o + row * p.num_splits * kHeadDim, nsplit,
               np ? p.prefix_lse + row * np : nullptr,
@@ -652,7 +663,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   if (tid == 0) *counter = 0u;  // ready for the next call
 }
 
-template <int G, int KVH, bool kMQ, bool kFp8 = false>
+template <int G, bool kMQ, bool kFp8 = false>
 int launch_g(const DecodeArgs& a, const DecodePlan& plan, const DecodeParams& prm,
              const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t stream) {
   using L = SmemLayout<G, kFp8>;
@@ -661,14 +672,14 @@ int launch_g(const DecodeArgs& a, const DecodePlan& plan, const DecodeParams& pr
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(paged_decode_kernel<G, KVH, kMQ, kFp8>,
+    if (cudaFuncSetAttribute(paged_decode_kernel<G, kMQ, kFp8>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::kBytes) != cudaSuccess)
       return PKV_ERR_LAUNCH;
     attr_set[dev] = true;
   }
-  dim3 grid(plan.num_splits, (a.Hkv / KVH) * plan.head_groups, a.B);
-  paged_decode_kernel<G, KVH, kMQ, kFp8><<<grid, kThreads, L::kBytes, stream>>>(km, vm, prm);
+  dim3 grid(plan.num_splits, a.Hkv * plan.head_groups, a.B);
+  paged_decode_kernel<G, kMQ, kFp8><<<grid, kThreads, L::kBytes, stream>>>(km, vm, prm);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }
 
@@ -686,11 +697,10 @@ int plan_decode(int B, int Hq, int Hkv, int max_blocks_per_seq, int num_splits,
   const int G = (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1;
   plan->heads_per_cta = G;
   plan->head_groups = g / G;
-  // One kv head per block.  (The kernel also reads KVH = 2 heads per block as
-  // 512-byte chunks per token; on GB300 that measured 2% slower on the
-  // batch-64 decode and slower on short contexts, so it is not selected.)
-  plan->kv_per_cta = 1;
-  const int kv_groups = Hkv / plan->kv_per_cta;
+  // One kv head per block.  (Reading two kv heads per block as 512-byte
+  // chunks per token measured 2% slower on GB300 on the batch-64 decode and
+  // slower on short contexts.)
+  const int kv_groups = Hkv;
   const int rest = max_blocks_per_seq - prefix_blocks;
   const int maxblk = rest > 0 ? rest : 1;
   int split_blocks;
@@ -753,13 +763,12 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
   if (a.B == 0) return PKV_OK;
   CUtensorMap km, vm;
   const int64_t slots = a.num_blocks * kBlockSize;
-  const int kvh = plan.kv_per_cta;
   if (a.fp8) {
     if (!encode_pool_map_u8(&km, a.k_cache, slots, a.Hkv, kTile) ||
         !encode_pool_map_u8(&vm, a.v_cache, slots, a.Hkv, kTile))
       return PKV_ERR_ARG;
-  } else if (!encode_pool_map(&km, a.k_cache, slots, a.Hkv, kTile / kvh, kvh) ||
-             !encode_pool_map(&vm, a.v_cache, slots, a.Hkv, kTile / kvh, kvh)) {
+  } else if (!encode_pool_map(&km, a.k_cache, slots, a.Hkv, kTile) ||
+             !encode_pool_map(&vm, a.v_cache, slots, a.Hkv, kTile)) {
     return PKV_ERR_ARG;
   }
   DecodeParams prm;
@@ -808,21 +817,21 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
   }
   if (a.fp8) {
     switch (plan.heads_per_cta) {
-      case 4: return launch_g<4, 1, false, true>(a, plan, prm, km, vm, stream);
-      case 2: return launch_g<2, 1, false, true>(a, plan, prm, km, vm, stream);
-      default: return launch_g<1, 1, false, true>(a, plan, prm, km, vm, stream);
+      case 4: return launch_g<4, false, true>(a, plan, prm, km, vm, stream);
+      case 2: return launch_g<2, false, true>(a, plan, prm, km, vm, stream);
+      default: return launch_g<1, false, true>(a, plan, prm, km, vm, stream);
     }
   }
   switch (plan.heads_per_cta) {
     case 4:
-      return a.q_len > 1 ? launch_g<4, 1, true>(a, plan, prm, km, vm, stream)
-                         : launch_g<4, 1, false>(a, plan, prm, km, vm, stream);
+      return a.q_len > 1 ? launch_g<4, true>(a, plan, prm, km, vm, stream)
+                         : launch_g<4, false>(a, plan, prm, km, vm, stream);
     case 2:
-      return a.q_len > 1 ? launch_g<2, 1, true>(a, plan, prm, km, vm, stream)
-                         : launch_g<2, 1, false>(a, plan, prm, km, vm, stream);
+      return a.q_len > 1 ? launch_g<2, true>(a, plan, prm, km, vm, stream)
+                         : launch_g<2, false>(a, plan, prm, km, vm, stream);
     default:
-      return a.q_len > 1 ? launch_g<1, 1, true>(a, plan, prm, km, vm, stream)
-                         : launch_g<1, 1, false>(a, plan, prm, km, vm, stream);
+      return a.q_len > 1 ? launch_g<1, true>(a, plan, prm, km, vm, stream)
+                         : launch_g<1, false>(a, plan, prm, km, vm, stream);
   }
 }
 

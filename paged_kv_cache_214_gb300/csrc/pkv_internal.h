@@ -76,7 +76,6 @@ struct DecodeArgs {
 
 // Split plan of one decode call.
 struct DecodePlan {
-  int kv_per_cta;     // KVH: kv heads one thread block reads (1, 2 or 4)
   int heads_per_cta;  // G: query heads per kv head that one thread block serves
   int head_groups;    // (Hq/Hkv) / G
   int split_blocks;   // whole KV blocks per split
