@@ -681,9 +681,10 @@ def run_verify_extra(pkv, dev, hbm_peak, flush, stream):
             "kv_tokens": kv_tokens, "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / hbm_peak, 4),
             "verified_tokens_per_s": round(w.B * qn / (med / 1e3), 1),
             "prefill_path_us": round(med_p * 1e3, 2),
-            "note": "paged_decode_attention_multiquery (tensor-core kernel, one (sequence, kv "
-                    "head) tile of g*q_len rows, K/V read once per kv head); prefill_path_us: "
-                    "the same batch through paged_prefill_attention (one tile per query head)"}
+            "note": "paged_decode_attention_multiquery: 8 (position, head) rows per kv head, "
+                    "all in one split-K decode block (K/V read once per kv head); "
+                    "prefill_path_us: the same batch through paged_prefill_attention (one "
+                    "tile per query head)"}
 
 
 def _traffic(workload: str, algorithmic: int):

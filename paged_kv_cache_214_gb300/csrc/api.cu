@@ -240,11 +240,14 @@ extern "C" int paged_decode_attention(void* out, float* lse, const void* q, cons
 constexpr int kMaxQueryLen = 64;
 
 // Multi-query decode on the tensor-core kernel (one item per (sequence, kv
-// head), all g*q_len rows in one tile) when the rows fit one tile and there
-// are at least as many items as SMs; otherwise (small batches, or a split
-// count the caller asks for) on the split-K decode kernel.
+// head), all g*q_len rows in one tile) when there are more rows per kv head
+// than one split-K decode block serves (8: it then reads K/V once too, and
+// measured faster), the rows fit one tile and there are at least as many
+// items as SMs; otherwise (up to 8 rows, small batches, or a split count the
+// caller asks for) on the split-K decode kernel.
 bool use_verify_kernel(int B, int q_len, int Hq, int Hkv, int num_splits) {
   if (num_splits != 0 || q_len < 2 || !verify_rows_fit(Hq / Hkv, q_len)) return false;
+  if ((Hq / Hkv) * q_len <= 8) return false;
   return static_cast<int64_t>(B) * Hkv >= device_sm_count();
 }
 

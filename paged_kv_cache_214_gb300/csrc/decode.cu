@@ -162,8 +162,11 @@ template <int G, bool kFp8 = false>
 struct SmemLayout {
   static constexpr int kStages = Geo<kFp8>::kStagesN;
   static constexpr int kStageBytes = Geo<kFp8>::kStageB;
-  static constexpr int kMergeO = kStages * kStageBytes;                      // [4][G][128] f32
-  static constexpr int kMergeM = kMergeO + kConsumerWarps * G * 128 * 4;     // [4][G]
+  // [4][G][128] f32, over the stage ring: written only once every warp is
+  // done with the stages and no copy is in flight
+  static constexpr int kMergeO = 0;
+  static_assert(kConsumerWarps * G * 128 * 4 <= kStages * kStageBytes, "merge buffer");
+  static constexpr int kMergeM = kStages * kStageBytes;                      // [4][G]
   static constexpr int kMergeL = kMergeM + kConsumerWarps * G * 4;           // [4][G]
   static constexpr int kBlk = kMergeL + kConsumerWarps * G * 4;              // [32] int
   static constexpr int kBars = kBlk + kMaxSplitBlocks * 4;                   // full[], empty[]
@@ -576,6 +579,18 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    __syncthreads();  // every warp is done with the stage ring
+    // After a timeout, wait (bounded) for copies still in flight before the
+    // ring's memory is written or the block's shared memory released.
+    if (flags[0] && tid == 0) {
+      const int issued = flags[2];
+      for (int s = 0; s < kStagesN; ++s) {
+        int last = -1;
+        for (int it = s; it < issued; it += kStagesN) last = it;
+        if (last >= 0) (void)mbar_wait(full_bar(s), (last / kStagesN) & 1);
+      }
+    }
+    __syncthreads();
     if (gq < G) {
       // this lane's output columns: n = 2c at dims 32c + jn and n = 2c + 1 at
       // dims 32c + 16 + jn (bf16: 32c + 16 + (jn ^ 8))
@@ -593,16 +608,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   }
 
   __syncthreads();
-  // After a timeout, wait (bounded) for copies still in flight before the
-  // block's shared memory can be released.
-  if (flags[0] && tid == 0) {
-    const int issued = flags[2];
-    for (int s = 0; s < kStagesN; ++s) {
-      int last = -1;
-      for (int it = s; it < issued; it += kStagesN) last = it;
-      if (last >= 0) (void)mbar_wait(full_bar(s), (last / kStagesN) & 1);
-    }
-  }
 
   // ---------------------------------------------------------------- epilogue
   // thread tid (0..127) owns dim d = tid of every head
@@ -694,7 +699,7 @@ int plan_decode(int B, int Hq, int Hkv, int max_blocks_per_seq, int num_splits,
     return PKV_ERR_ARG;
   if (Hq % Hkv) return PKV_ERR_SHAPE;
   const int g = Hq / Hkv;
-  const int G = (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1;
+  const int G = (g % 8 == 0) ? 8 : (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1;
   plan->heads_per_cta = G;
   plan->head_groups = g / G;
   // One kv head per block.  (Reading two kv heads per block as 512-byte
@@ -817,12 +822,16 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
   }
   if (a.fp8) {
     switch (plan.heads_per_cta) {
+      case 8: return launch_g<8, false, true>(a, plan, prm, km, vm, stream);
       case 4: return launch_g<4, false, true>(a, plan, prm, km, vm, stream);
       case 2: return launch_g<2, false, true>(a, plan, prm, km, vm, stream);
       default: return launch_g<1, false, true>(a, plan, prm, km, vm, stream);
     }
   }
   switch (plan.heads_per_cta) {
+    case 8:
+      return a.q_len > 1 ? launch_g<8, true>(a, plan, prm, km, vm, stream)
+                         : launch_g<8, false>(a, plan, prm, km, vm, stream);
     case 4:
       return a.q_len > 1 ? launch_g<4, true>(a, plan, prm, km, vm, stream)
                          : launch_g<4, false>(a, plan, prm, km, vm, stream);

@@ -51,7 +51,7 @@ def test_forced_splits(num_splits):
     run_and_check(w, num_splits=num_splits, what=f"S={num_splits}")
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 8), (32, 8), (24, 8), (64, 8), (4, 1), (14, 2)])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 8), (32, 8), (24, 8), (64, 8), (4, 1), (14, 2), (16, 1)])
 def test_head_groupings(Hq, Hkv):
     lens = [5, 64, 130, 700, 2000]
     w = W.make_decode(lens, Hq, Hkv, 24, 2000 + Hq * 10 + Hkv)

@@ -51,6 +51,14 @@ def tensor_core_path(w, q_len):
         w.B, q_len, w.Hq, w.Hkv, w.D, w.block_tables.shape[1]) == 0
 
 
+def expect_tensor_core(w, q_len):
+    """The routing rule: the tensor-core kernel takes batches of at least one
+    (sequence, kv head) item per SM with more than 8 (position, head) rows per
+    kv head; up to 8 rows fit one split-K decode block, which reads K/V once."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return w.B * w.Hkv >= sms and (w.Hq // w.Hkv) * q_len > 8
+
+
 # 24 ragged sequences (across block and tile boundaries, some holding nothing
 # but the new tokens): 24 x 8 kv heads = 192 items, the tensor-core path
 CACHED_24 = [0, 1, 63, 64, 127, 128, 255, 256, 300, 511, 512, 700,
@@ -59,10 +67,12 @@ CACHED_24 = [0, 1, 63, 64, 127, 128, 255, 256, 300, 511, 512, 700,
 
 @pytest.mark.parametrize("q_len", [2, 4, 8])
 @pytest.mark.parametrize("Hq,Hkv", [(16, 8), (32, 8), (8, 8), (24, 8)])
-def test_verify_tensor_core_path(q_len, Hq, Hkv):
+def test_verify_large_batch(q_len, Hq, Hkv):
+    # 192 items: the tensor-core kernel for more than 8 rows per kv head,
+    # the split-K decode kernel (all rows in one block) otherwise
     w = verify_batch(CACHED_24, q_len, Hq, Hkv, 512, 7000 + 10 * q_len + Hq)
-    assert tensor_core_path(w, q_len)
-    run_and_check(w, q_len, what=f"tcgen05 q_len={q_len} Hq={Hq} Hkv={Hkv}")
+    assert tensor_core_path(w, q_len) == expect_tensor_core(w, q_len)
+    run_and_check(w, q_len, what=f"q_len={q_len} Hq={Hq} Hkv={Hkv}")
 
 
 @pytest.mark.parametrize("q_len", [2, 4, 8])
@@ -121,9 +131,11 @@ def test_context_shorter_than_q_len_is_reported():
     assert pkv.get_device_error() == pkv.PKV_OK   # reading clears it
 
 
-def test_verify_batch_of_decode_size():
-    # batch-64 verify of 4 proposed tokens over contexts like the decode bench
+@pytest.mark.parametrize("q_len", [4, 8])
+def test_verify_batch_of_decode_size(q_len):
+    # batch-64 verify of q_len proposed tokens over contexts like the decode
+    # bench: 8 rows per kv head on the split-K decode kernel, 16 on tcgen05
     lens = W._uniform_ints(512, 4096, 64, W.seed_for(2))
-    w = verify_batch([L - 4 for L in lens], 4, 16, 8, 1200, 7400)
-    assert tensor_core_path(w, 4)
-    run_and_check(w, 4, what="b64 verify")
+    w = verify_batch([L - q_len for L in lens], q_len, 16, 8, 1200, 7400 + q_len)
+    assert tensor_core_path(w, q_len) == (q_len == 8)
+    run_and_check(w, q_len, what=f"b64 verify q_len={q_len}")
