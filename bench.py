@@ -3,15 +3,17 @@
 One step = one decode step of one attention layer over the batch-64 decode
 workload (64 sequences, 16 query / 8 kv heads, head_dim 128, 256-token blocks,
 context lengths uniform in [512, 4096], physical blocks shuffled in a 2048-block
-pool): kv_cache_store of the 64 new tokens, then paged_decode_attention.
+pool): the store of the 64 new tokens and the decode, in one launch
+(paged_decode_attention_store); the same steps as two launches
+(kv_cache_store, then paged_decode_attention) are timed beside it.
 
-Inputs larger than L2: each step reads about 604 MB of K/V (L2 is ~129 MB), and
+Inputs larger than L2: each step reads about 524 MB of K/V (L2 is ~129 MB), and
 consecutive steps cycle through three batches whose blocks are disjoint, so no
 step finds the previous step's K/V in L2.
 
 Prints one JSON line (rank 0).  `value` is algorithmic HBM bytes per step
 (store + decode, see DESIGN notes) x steps / device time, in GB/s; the same line
-carries KV-tokens/s, the roofline of the dominant kernel (decode), the oracle
+carries KV-tokens/s, the roofline of the step's kernel, the oracle
 timed on the host cores (`cpu_baseline`), an end-to-end number through the
 public API with host buffers (`e2e`), clocks sampled during the timed region
 and extra measurements of the other workloads.
@@ -260,6 +262,14 @@ def time_oracle(w, budget_s: float = 12.0, n_seq: int = None):
 
 
 def _decode_step(pkv, w, dev_inputs, r, ws, out, lse, stream):
+    """One step: store of the new tokens and decode, in one launch."""
+    q, kn, vn, kc, vc, tables, slots, lens = dev_inputs
+    pkv.paged_decode_attention_store(q, kn, vn, slots[r], kc, vc, tables[r], lens, w.scale,
+                                     out=out, lse=lse, workspace=ws, stream=stream)
+
+
+def _decode_step_two_calls(pkv, w, dev_inputs, r, ws, out, lse, stream):
+    """The same step as kv_cache_store followed by paged_decode_attention."""
     q, kn, vn, kc, vc, tables, slots, lens = dev_inputs
     pkv.kv_cache_store(kn, vn, kc, vc, slots[r], stream=stream)
     pkv.paged_decode_attention(q, kc, vc, tables[r], lens, w.scale, out=out, lse=lse,
@@ -304,32 +314,41 @@ def run_gpu(args, world, rank):
     if rank == 0:
         clocks.start()
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
+    # A step is one launch (store + decode), so the launches run back to back
+    # and their average duration is the timed region over K: no event sits
+    # between two launches to stretch the step.
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     start.record(stream)
     for i in range(K):
-        r = i % R
-        pkv.kv_cache_store(kn, vn, kc, vc, slots[r], stream=stream)
-        ev[i][0].record(stream)
-        pkv.paged_decode_attention(q, kc, vc, tables[r], lens, w.scale, out=out, lse=lse,
-                                   workspace=ws, stream=stream)
-        ev[i][1].record(stream)
+        _decode_step(pkv, w, dev_inputs, i % R, ws, out, lse, stream)
     end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop() if rank == 0 else None
     elapsed_ms = start.elapsed_time(end)
     elapsed_ms = max_over_ranks(elapsed_ms, world)
-    dec_ms = [a.elapsed_time(b) for a, b in ev]
-    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    dec_avg_ms = start.elapsed_time(end) / K   # this rank's own launches
     assert pkv.get_device_error() == pkv.PKV_OK
 
     value = step_bytes * K * world / (elapsed_ms / 1e3) / 1e9
     kv_tps = w.kv_tokens * K * world / (elapsed_ms / 1e3)
-    dec_gbs = dec_bytes / (dec_avg_ms / 1e3) / 1e9
+    # the step's one kernel: the new tokens' store and the decode
+    dec_gbs = step_bytes / (dec_avg_ms / 1e3) / 1e9
+
+    # for comparison: the same steps as two launches (store, then decode)
+    for i in range(3):
+        _decode_step_two_calls(pkv, w, dev_inputs, i % R, ws, out, lse, stream)
+    a2, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a2.record(stream)
+    for i in range(K):
+        _decode_step_two_calls(pkv, w, dev_inputs, i % R, ws, out, lse, stream)
+    b2.record(stream)
+    torch.cuda.synchronize()
+    two_ms = a2.elapsed_time(b2) / K
+    assert pkv.get_device_error() == pkv.PKV_OK
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -343,14 +362,17 @@ def run_gpu(args, world, rank):
                          f"{R} rotating batches with disjoint blocks"},
         "kv_tokens_per_s": round(kv_tps, 1),
         "pct_of_peak_hbm": round(100 * value / hbm_peak, 2),
-        "gpu_launches": 2 * K,
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel",
+        "gpu_launches": K,
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel (store fused)",
                      "achieved": round(dec_gbs, 1), "peak": hbm_peak,
                      "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
                      "frac": round(dec_gbs / hbm_peak, 4),
-                     "traffic": _traffic("decode-b64", dec_bytes),
-                     "algorithmic_bytes_per_launch": dec_bytes,
+                     "traffic": _traffic("decode-b64", step_bytes),
+                     "algorithmic_bytes_per_launch": step_bytes,
                      "avg_launch_us": round(dec_avg_ms * 1e3, 2)},
+        "two_launch_step": {"ms_per_step": round(two_ms, 5),
+                            "value": round(step_bytes / (two_ms / 1e3) / 1e9, 2),
+                            "note": "kv_cache_store + paged_decode_attention"},
         "clocks": clk,
     }
     if rank == 0 and not args.profile:
@@ -374,8 +396,8 @@ def _trimmed_decode_b64(dev):
 
 def run_e2e(pkv, w, dev_inputs, ws, stream, K, step_bytes):
     """Same step through the public API with the step's inputs in pinned host
-    memory: H2D copies of q, new K/V, slots, tables and lengths, store + decode,
-    D2H copy of out and lse, all inside the timed region."""
+    memory: H2D copies of q, new K/V, slots, tables and lengths, the fused store
+    + decode, D2H copy of out and lse, all inside the timed region."""
     q, kn, vn, kc, vc, tables, slots, lens = dev_inputs
     R = len(tables)
     h_q = w.q.pin_memory()
@@ -402,9 +424,9 @@ def run_e2e(pkv, w, dev_inputs, ws, stream, K, step_bytes):
         d_tab.copy_(h_tables[r], non_blocking=True)
         d_slot.copy_(h_slots[r], non_blocking=True)
         d_lens.copy_(h_lens, non_blocking=True)
-        pkv.kv_cache_store(d_k, d_v, kc, vc, d_slot, stream=stream)
-        pkv.paged_decode_attention(d_q, kc, vc, d_tab, d_lens, w.scale, out=d_out, lse=d_lse,
-                                   workspace=ws, stream=stream)
+        pkv.paged_decode_attention_store(d_q, d_k, d_v, d_slot, kc, vc, d_tab, d_lens,
+                                         w.scale, out=d_out, lse=d_lse, workspace=ws,
+                                         stream=stream)
         h_out.copy_(d_out, non_blocking=True)
         h_lse.copy_(d_lse, non_blocking=True)
 

@@ -150,6 +150,33 @@ int paged_decode_attention(void* out, float* lse, const void* q,
                            void* workspace, size_t workspace_bytes,
                            int num_splits, pkv_stream_t stream);
 
+/* paged_decode_attention_store — kv_cache_store of the step's new tokens and
+ * paged_decode_attention over the updated cache in one launch, the way the
+ * attention layer stores K/V through slot_mapping and then attends
+ * (Nano-vLLM System Architecture Analysis, §2 Core Components, "Attention
+ * with Paged Cache").  Results equal kv_cache_store(k_new, v_new, ...,
+ * slot_mapping) followed by paged_decode_attention(...) with the same
+ * arguments, under one more rule: slot_mapping[b] is -1 (nothing stored) or
+ * the slot of sequence b's last position, context_lens[b] - 1, through its
+ * block table.  Any other slot is not written and is reported as
+ * PKV_ERR_DEVICE_INDEX through pkv_get_device_error().  The blocks that
+ * attend over a sequence's last range write its new row, one kv head each,
+ * before they read that range; no other block reads that position, so no
+ * block waits for another.
+ * k_new, v_new : bf16 [B, Hkv, D] rows, token strides k_tok_stride /
+ *   v_tok_stride in elements (multiples of 8, >= Hkv*D), 16-byte aligned.
+ * slot_mapping : int32 [B] on the device.  Pools are written; everything else
+ * (layouts, workspace = paged_decode_workspace_bytes of the same shapes,
+ * results, errors) as paged_decode_attention. */
+int paged_decode_attention_store(void* out, float* lse, const void* q, const void* k_new,
+                                 const void* v_new, int64_t k_tok_stride, int64_t v_tok_stride,
+                                 const int32_t* slot_mapping, void* k_cache, void* v_cache,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* context_lens, int B, int Hq, int Hkv, int D,
+                                 int block_size, int64_t num_blocks, float scale,
+                                 void* workspace, size_t workspace_bytes, int num_splits,
+                                 pkv_stream_t stream);
+
 /* paged_decode_shared_prefix_workspace_bytes — workspace bytes that a
  * paged_decode_attention_shared_prefix call with the same arguments needs
  * (0 for arguments that call would reject). */

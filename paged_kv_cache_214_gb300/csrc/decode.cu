@@ -88,6 +88,14 @@ struct DecodeParams {
   int prefix_splits;        // partials per row of the shared-prefix pass
   const float* prefix_o;    // [B*Hq, prefix_splits, 128]
   const float* prefix_lse;  // [B*Hq, prefix_splits] log2-sum-exp
+  // Fused store (bf16 pools; new_slots == nullptr: none): the new token of
+  // sequence b, rows k_new / v_new + b * stride, goes to slot new_slots[b].
+  const int32_t* new_slots;
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  int64_t k_new_stride, v_new_stride;  // elements
+  uint4* k_pool;                       // the pools, writable
+  uint4* v_pool;
 };
 
 // Log-sum-exp merge of one output row by one warp: nsplit partials
@@ -170,7 +178,7 @@ struct SmemLayout {
   static constexpr int kMergeL = kMergeM + kConsumerWarps * G * 4;           // [4][G]
   static constexpr int kBlk = kMergeL + kConsumerWarps * G * 4;              // [32] int
   static constexpr int kBars = kBlk + kMaxSplitBlocks * 4;                   // full[], empty[]
-  static constexpr int kFlags = kBars + 2 * kStages * 8;                     // abort, last, issued
+  static constexpr int kFlags = kBars + (2 * kStages + 1) * 8;  // + stored; abort, last, issued
   static constexpr int kEnd = kFlags + 16;
   static constexpr int kBytes = kEnd + 1024;                                 // + alignment slack
 };
@@ -204,6 +212,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   const uint32_t bars = smem_addr(smem + L::kBars);
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (kStagesN + s); };
+  const uint32_t stored_bar = bars + 8u * (2 * kStagesN);  // fused store: the new row written
 
   const int split = blockIdx.x;
   const int hg = blockIdx.y;  // kv head * head_groups + query head group
@@ -248,6 +257,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   const int nsplit = (ctx - P + split_tokens - 1) / split_tokens;
   if (split >= (nsplit > 0 ? nsplit : 1)) return;  // whole block exits: no work
 
+  // Fused store: the blocks of a sequence's last range write the step's new
+  // token (see below); a sequence with no token to attend takes none.
+  const bool store_here =
+      !kFp8 && p.new_slots != nullptr && split == (nsplit > 0 ? nsplit : 1) - 1;
+  if (store_here && ctx == P && tid == 0 && __ldg(p.new_slots + b) >= 0)
+    record_error(p.err, kErrIndex);
+
   if (P > 0 && split == 0 && hg == 0 && warp == 0) {
     // the shared prefix must be the same physical blocks as sequence 0's
     const int32_t* row = p.block_tables + static_cast<int64_t>(b) * p.maxblk;
@@ -290,6 +306,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     const int s = it % kStagesN;
     const int tok = tok_begin + it * kTile;
     const int slot = sblk[tok / kBlockSize - blk_begin] * kBlockSize + tok % kBlockSize;
+    // the tile holding the new token is read only once that token is written
+    if (store_here && it == n_tiles - 1 && !mbar_wait(stored_bar, 0)) {
+      record_error(p.err, kErrTimeout);
+      flags[0] = 1;
+      return;
+    }
     if constexpr (kFp8) {
       // warp 0: the K tile, warp 1: the V tile (one 128-byte-wide box each)
       const uint32_t dst = smem_addr(smem + s * kStageB) + warp * kOpBytes;
@@ -314,6 +336,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         mbar_init(full_bar(s), kIssuers);         // one arrival per issuing warp
         mbar_init(empty_bar(s), kConsumerWarps);
       }
+      mbar_init(stored_bar, 1);
       flags[0] = 0;  // abort
       flags[1] = 0;  // last-arrival flag
       flags[2] = 0;  // tiles issued
@@ -331,6 +354,31 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     }
   }
   __syncthreads();
+  if (store_here && warp == 1) {
+    // Warp 1 writes the new token's row of this kv head (lanes 0-15 K, 16-31
+    // V) at its slot, which must be the slot of position ctx - 1: no other
+    // range reads it, and blocks of other head groups write the same bytes.
+    // Any other slot is reported and not written.  Then it tells the issuing
+    // lanes, one of which waits for it before copying the tile that holds it.
+    const int sl = __ldg(p.new_slots + b);
+    if (sl >= 0) {
+      const int pos = ctx - 1;
+      const int blk = sblk[pos / kBlockSize - blk_begin];
+      if (sl == blk * kBlockSize + pos % kBlockSize) {
+        const __nv_bfloat16* row = lane < 16 ? p.k_new + b * p.k_new_stride
+                                             : p.v_new + b * p.v_new_stride;
+        const uint4 v =
+            __ldg(reinterpret_cast<const uint4*>(row + kvh0 * kHeadDim) + (lane & 15));
+        uint4* pool = lane < 16 ? p.k_pool : p.v_pool;
+        pool[(static_cast<int64_t>(sl) * p.Hkv + kvh0) * (kHeadDim / 8) + (lane & 15)] = v;
+        fence_proxy_async_global();
+      } else if (lane == 0) {
+        record_error(p.err, kErrIndex);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(stored_bar);
+  }
   if (lane == 0 && warp < kIssuers)
     for (int it = 0; it < kStagesN && it < n_tiles; ++it) issue(it);
 
@@ -798,6 +846,13 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
   prm.scale_log2 = a.scale * 1.4426950408889634f;
   prm.prefix_tokens = a.prefix_tokens;
   prm.prefix_splits = plan.prefix_splits;
+  prm.new_slots = a.new_slots;
+  prm.k_new = static_cast<const __nv_bfloat16*>(a.k_new);
+  prm.v_new = static_cast<const __nv_bfloat16*>(a.v_new);
+  prm.k_new_stride = a.k_new_stride;
+  prm.v_new_stride = a.v_new_stride;
+  prm.k_pool = static_cast<uint4*>(const_cast<void*>(a.k_cache));
+  prm.v_pool = static_cast<uint4*>(const_cast<void*>(a.v_cache));
   prm.prefix_o = nullptr;
   prm.prefix_lse = nullptr;
   if (a.prefix_tokens > 0) {

@@ -267,6 +267,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// This thread's generic-proxy writes to global memory are ordered before
+// later async-proxy (TMA) reads of the same bytes (after a block barrier, by
+// any thread of the block).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // 32 consecutive columns of this thread's TMEM lane -> 32 registers.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(

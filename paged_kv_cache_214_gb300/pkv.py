@@ -76,6 +76,10 @@ def load_library(path: str = LIB_PATH):
         lib.paged_decode_attention_multiquery.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32,
                                                           i32, i32, i32, i64, f32, P, sz, i32, P]
         lib.paged_decode_attention_multiquery.restype = i32
+        lib.paged_decode_attention_store.argtypes = [P, P, P, P, P, i64, i64, P, P, P, P, i32,
+                                                     P, i32, i32, i32, i32, i32, i64, f32, P,
+                                                     sz, i32, P]
+        lib.paged_decode_attention_store.restype = i32
         lib.kv_cache_store_fp8.argtypes = [P, P, i64, i64, P, P, P, i64, i32, i32, i32, i64,
                                            f32, f32, P]
         lib.kv_cache_store_fp8.restype = i32
@@ -236,6 +240,49 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                                       _ptr(context_lens), B, Hq, Hkv, D, bs, NB, float(scale),
                                       _ptr(workspace), ws_bytes, int(num_splits),
                                       _stream(stream)), "paged_decode_attention")
+    return out, lse
+
+
+def paged_decode_attention_store(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                                 slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                                 v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                 context_lens: torch.Tensor, scale: float,
+                                 out: Optional[torch.Tensor] = None,
+                                 lse: Optional[torch.Tensor] = None,
+                                 workspace: Optional[torch.Tensor] = None, num_splits: int = 0,
+                                 want_lse: bool = True, stream=None
+                                 ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Store the step's new tokens (k_new / v_new bf16 [B, Hkv, D] at
+    slot_mapping[b], which must be -1 or the slot of position
+    context_lens[b] - 1) and decode, in one launch.  Returns (out, lse) as
+    paged_decode_attention."""
+    lib = load_library()
+    NB, bs, Hkv, D = _pool_dims(k_cache, v_cache)
+    _need(q, "q", torch.bfloat16, 3)
+    B, Hq, Dq = q.shape
+    if Dq != D:
+        raise ValueError("q head_dim differs from the cache's")
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        _need(t, name, torch.bfloat16, 3, contiguous=False)
+        if tuple(t.shape) != (B, Hkv, D) or t.stride(2) != 1 or t.stride(1) != D:
+            raise ValueError(f"{name} must be [B, {Hkv}, {D}] with contiguous rows")
+    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    maxblk = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    need = paged_decode_workspace_bytes(B, Hq, Hkv, D, maxblk, bs, num_splits)
+    if workspace is None and need:
+        workspace = decode_workspace(need, q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.paged_decode_attention_store(
+        _ptr(out), _ptr(lse), _ptr(q), _ptr(k_new), _ptr(v_new), k_new.stride(0),
+        v_new.stride(0), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        maxblk, _ptr(context_lens), B, Hq, Hkv, D, bs, NB, float(scale), _ptr(workspace),
+        ws_bytes, int(num_splits), _stream(stream)), "paged_decode_attention_store")
     return out, lse
 
 

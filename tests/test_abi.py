@@ -109,6 +109,27 @@ def test_fp8_host_checks(lib):
                 0.5, None, 0, 0, s) == pkv.PKV_ERR_ARG
 
 
+def test_decode_store_host_checks(lib):
+    s = None
+    ds = lib.paged_decode_attention_store
+    P = 16  # a stand-in device address: the checks below fail before any use
+    # nothing to do
+    assert ds(None, None, None, None, None, 1024, 1024, None, None, None, None, 1, None, 0, 16,
+              8, 128, 256, 4, 1.0, None, 0, 0, s) == pkv.PKV_OK
+    # shapes, then missing pointers
+    assert ds(None, None, None, None, None, 1024, 1024, None, None, None, None, 1, None, 2, 12,
+              8, 128, 256, 4, 1.0, None, 0, 0, s) == pkv.PKV_ERR_SHAPE
+    assert ds(None, None, None, None, None, 1024, 1024, None, None, None, None, 1, None, 2, 16,
+              8, 128, 256, 4, 1.0, None, 0, 0, s) == pkv.PKV_ERR_ARG
+    # token strides: at least Hkv * D and a multiple of 8 elements
+    for ks in (1000, 1028):
+        assert ds(P, None, P, P, P, ks, 1024, P, P, P, P, 1, P, 2, 16, 8, 128, 256, 4, 1.0, None,
+                  0, 0, s) == pkv.PKV_ERR_ARG
+    # a misaligned new-token row
+    assert ds(P, None, P, P + 2, P, 1024, 1024, P, P, P, P, 1, P, 2, 16, 8, 128, 256, 4, 1.0,
+              None, 0, 0, s) == pkv.PKV_ERR_ARG
+
+
 def test_workspace_query_and_split_plan(lib):
     # one split needs no workspace; several need partials + counters
     assert pkv.paged_decode_workspace_bytes(4, 16, 8, 128, 1, 256, 1) == 0
