@@ -227,11 +227,33 @@ def _sample_decode_bytes(w, seqs):
             sum(-(-int(w.context_lens[s]) // w.block_size) for s in seqs) * 4 + n * 4)
 
 
-def oracle_step(s, scale):
+def oracle_step(s, scale, nthreads=0):
     import oracle
     kc, vc = s["kc"].copy(), s["vc"].copy()
     oracle.store(s["k"], s["v"], kc, vc, s["slots"])
-    oracle.decode(s["q"], kc, vc, s["tables"], s["lens"], scale)
+    oracle.decode(s["q"], kc, vc, s["tables"], s["lens"], scale, nthreads=nthreads)
+
+
+def time_oracle_single_core(dev, budget_s: float = 2.0):
+    """The oracle on one thread: tiny-decode whole, decode-b64 on its first 4
+    sequences; store + decode GB/s of each sample."""
+    res = {}
+    for cfg, n_seq in ((1, None), (2, 4)):
+        w = W.config_workload(cfg, pool_device=dev)
+        s = oracle_sample(w, n_seq or w.B)
+        t0 = time.perf_counter()
+        oracle_step(s, w.scale, nthreads=1)
+        one = time.perf_counter() - t0
+        reps = max(1, int(budget_s / max(one, 1e-4)))
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            oracle_step(s, w.scale, nthreads=1)
+        el = time.perf_counter() - t0
+        res[w.name] = {"GB/s": round(s["bytes"] * reps / el / 1e9, 4),
+                       "kv_tokens_per_s": round(s["tokens"] * reps / el, 1),
+                       "sample": f"{n_seq or w.B} of {w.B} sequences, {reps} passes"}
+        del w
+    return res
 
 
 def time_oracle(w, budget_s: float = 12.0, n_seq: int = None):
@@ -384,6 +406,7 @@ def run_gpu(args, world, rank):
             result["extras"] = run_extras(pkv, dev, hbm_peak, args)
         if not args.no_cpu_baseline:
             result["cpu_baseline"] = time_oracle(W.config_workload(2, pool_device=dev))
+            result["cpu_baseline"]["single_core"] = time_oracle_single_core(dev)
     return result
 
 
@@ -483,10 +506,10 @@ def run_extras(pkv, dev, hbm_peak, args):
         def call():
             pkv.paged_decode_attention(q, kc, vc, tables, lens, w.scale, out=out, lse=lse,
                                        workspace=ws, stream=stream)
-        for _ in range(5):
+        for _ in range(10):
             call()
         times = []
-        for _ in range(30):
+        for _ in range(50):
             _flush_l2(flush)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -519,10 +542,10 @@ def run_extras(pkv, dev, hbm_peak, args):
                 pkv.paged_decode_attention_shared_prefix(q, kc, vc, tables, lens, w.scale, P,
                                                          out=out, lse=lse, workspace=ws2,
                                                          stream=stream)
-            for _ in range(5):
+            for _ in range(10):
                 call_sp()
             times = []
-            for _ in range(30):
+            for _ in range(50):
                 _flush_l2(flush)
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
@@ -578,7 +601,7 @@ def run_extras(pkv, dev, hbm_peak, args):
     lse = torch.empty((q.shape[0], w.Hq), dtype=torch.float32, device=dev)
     entry = {"workload": w.name}
     st_med, _ = _time_calls(lambda: pkv.kv_cache_store(kn, vn, kc, vc, slots, stream=stream),
-                            30, stream)
+                            50, stream)
     sb = store_bytes(q.shape[0], w.Hkv, w.D)
     entry["store_us"] = round(st_med * 1e3, 2)
     entry["store_GB/s"] = round(sb / (st_med / 1e3) / 1e9, 1)
@@ -586,9 +609,9 @@ def run_extras(pkv, dev, hbm_peak, args):
         def pcall():
             pkv.paged_prefill_attention(q, kc, vc, tables, cq, ck, w.max_seqlen_q,
                                         w.max_seqlen_k, w.scale, out=out, lse=lse, stream=stream)
-        for _ in range(3):
+        for _ in range(10):
             pcall()
-        med, mn = _time_calls(pcall, 20, stream)
+        med, mn = _time_calls(pcall, 50, stream)
         fl = prefill_flops(w)
         _, bf16_peak, kind = _peaks()
         entry.update({"prefill_us": round(med * 1e3, 2), "prefill_min_us": round(mn * 1e3, 2),
@@ -632,10 +655,10 @@ def run_fp8_extra(pkv, dev, hbm_peak, flush, stream, cfg):
     def call():
         pkv.paged_decode_attention_fp8(q, k8, v8, tables, lens, w.scale, ks, vs, out=out,
                                        lse=lse, workspace=ws, stream=stream)
-    for _ in range(5):
+    for _ in range(10):
         call()
     times = []
-    for _ in range(30):
+    for _ in range(50):
         _flush_l2(flush)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -675,10 +698,10 @@ def run_verify_extra(pkv, dev, hbm_peak, flush, stream):
     ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
 
     def timed(fn):
-        for _ in range(5):
+        for _ in range(10):
             fn()
         times = []
-        for _ in range(30):
+        for _ in range(50):
             _flush_l2(flush)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
