@@ -319,6 +319,23 @@ int paged_decode_attention_fp8(void* out, float* lse, const void* q, const void*
                                float scale, float k_scale, float v_scale, void* workspace,
                                size_t workspace_bytes, int num_splits, pkv_stream_t stream);
 
+/* paged_decode_attention_fp8_store — kv_cache_store_fp8 of the step's new
+ * tokens and paged_decode_attention_fp8 over the updated pools in one launch,
+ * as paged_decode_attention_store is for bf16 pools: the same slot rule
+ * (slot_mapping[b] is -1 or the slot of position context_lens[b] - 1; any
+ * other slot is reported and not written), the same quantization as
+ * kv_cache_store_fp8, results bit-identical to the two calls.  Arguments as
+ * paged_decode_attention_store plus k_scale, v_scale (finite, > 0). */
+int paged_decode_attention_fp8_store(void* out, float* lse, const void* q, const void* k_new,
+                                     const void* v_new, int64_t k_tok_stride,
+                                     int64_t v_tok_stride, const int32_t* slot_mapping,
+                                     void* k_cache, void* v_cache, const int32_t* block_tables,
+                                     int max_blocks_per_seq, const int32_t* context_lens, int B,
+                                     int Hq, int Hkv, int D, int block_size, int64_t num_blocks,
+                                     float scale, float k_scale, float v_scale, void* workspace,
+                                     size_t workspace_bytes, int num_splits,
+                                     pkv_stream_t stream);
+
 /* paged_prefill_attention — causal prefill / chunked prefill with a prefix
  * cache: "During prefill with prefix cache, gathers cached K/V from the paged
  * cache and concatenates with newly computed ones" (Nano-vLLM System

@@ -279,6 +279,50 @@ extern "C" int paged_decode_attention_store(
   return launch_decode(a, plan, err, reinterpret_cast<cudaStream_t>(stream));
 }
 
+extern "C" int paged_decode_attention_fp8_store(
+    void* out, float* lse, const void* q, const void* k_new, const void* v_new,
+    int64_t k_tok_stride, int64_t v_tok_stride, const int32_t* slot_mapping, void* k_cache,
+    void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* context_lens, int B, int Hq, int Hkv, int D, int block_size,
+    int64_t num_blocks, float scale, float k_scale, float v_scale, void* workspace,
+    size_t workspace_bytes, int num_splits, pkv_stream_t stream) {
+  if (B < 0 || Hq <= 0 || max_blocks_per_seq < 0 || num_splits < 0) return PKV_ERR_ARG;
+  if (!valid_scale(k_scale) || !valid_scale(v_scale)) return PKV_ERR_ARG;
+  int st = check_pool(Hkv, D, block_size, num_blocks);
+  if (st) return st;
+  if (Hq % Hkv) return PKV_ERR_SHAPE;
+  if (B == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !context_lens || !k_new || !v_new || !slot_mapping)
+    return PKV_ERR_ARG;
+  if (max_blocks_per_seq > 0 && !block_tables) return PKV_ERR_ARG;
+  if (num_blocks == 0 && max_blocks_per_seq > 0) return PKV_ERR_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(k_new) || !aligned16(v_new))
+    return PKV_ERR_ARG;
+  const int64_t row = static_cast<int64_t>(Hkv) * D;
+  if (k_tok_stride < row || v_tok_stride < row || k_tok_stride % 8 || v_tok_stride % 8)
+    return PKV_ERR_ARG;
+  DecodePlan plan;
+  st = plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), 0, &plan);
+  if (st) return st;
+  if (plan.workspace_bytes) {
+    if (!workspace || workspace_bytes < plan.workspace_bytes ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+      return PKV_ERR_WORKSPACE;
+  }
+  unsigned* err = device_error_word();
+  if (!err) return PKV_ERR_LAUNCH;
+  DecodeArgs a{out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+               B, Hq, Hkv, num_blocks, scale, workspace, workspace_bytes, num_splits, 0, 1,
+               1, k_scale, v_scale};
+  a.new_slots = slot_mapping;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.k_new_stride = k_tok_stride;
+  a.v_new_stride = v_tok_stride;
+  return launch_decode(a, plan, err, reinterpret_cast<cudaStream_t>(stream));
+}
+
 // Longest run of query positions per sequence the multi-query decode accepts.
 constexpr int kMaxQueryLen = 64;
 

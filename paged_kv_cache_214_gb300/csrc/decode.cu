@@ -96,6 +96,7 @@ struct DecodeParams {
   int64_t k_new_stride, v_new_stride;  // elements
   uint4* k_pool;                       // the pools, writable
   uint4* v_pool;
+  float k_inv, v_inv;                  // E4M3 pools: binary32 1/k_scale, 1/v_scale
 };
 
 // Log-sum-exp merge of one output row by one warp: nsplit partials
@@ -259,8 +260,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 
   // Fused store: the blocks of a sequence's last range write the step's new
   // token (see below); a sequence with no token to attend takes none.
-  const bool store_here =
-      !kFp8 && p.new_slots != nullptr && split == (nsplit > 0 ? nsplit : 1) - 1;
+  const bool store_here = p.new_slots != nullptr && split == (nsplit > 0 ? nsplit : 1) - 1;
   if (store_here && ctx == P && tid == 0 && __ldg(p.new_slots + b) >= 0)
     record_error(p.err, kErrIndex);
 
@@ -355,23 +355,52 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   }
   __syncthreads();
   if (store_here && warp == 1) {
-    // Warp 1 writes the new token's row of this kv head (lanes 0-15 K, 16-31
-    // V) at its slot, which must be the slot of position ctx - 1: no other
-    // range reads it, and blocks of other head groups write the same bytes.
-    // Any other slot is reported and not written.  Then it tells the issuing
-    // lanes, one of which waits for it before copying the tile that holds it.
+    // Warp 1 writes the new token's row of this kv head at its slot, which
+    // must be the slot of position ctx - 1: no other range reads it, and
+    // blocks of other head groups write the same bytes.  Any other slot is
+    // reported and not written.  bf16: lanes 0-15 copy the K row, 16-31 the V
+    // row, 16 bytes each.  E4M3: lanes 0-7 quantize 16 elements of the K row,
+    // 8-15 of the V row, exactly as kv_cache_store_fp8 does (fp32 product with
+    // the binary32 reciprocal scale, nearest code, ties to even, saturating).
+    // Then the warp tells the issuing lanes, one of which waits for it before
+    // copying the tile that holds the row.
     const int sl = __ldg(p.new_slots + b);
     if (sl >= 0) {
       const int pos = ctx - 1;
       const int blk = sblk[pos / kBlockSize - blk_begin];
       if (sl == blk * kBlockSize + pos % kBlockSize) {
-        const __nv_bfloat16* row = lane < 16 ? p.k_new + b * p.k_new_stride
-                                             : p.v_new + b * p.v_new_stride;
-        const uint4 v =
-            __ldg(reinterpret_cast<const uint4*>(row + kvh0 * kHeadDim) + (lane & 15));
-        uint4* pool = lane < 16 ? p.k_pool : p.v_pool;
-        pool[(static_cast<int64_t>(sl) * p.Hkv + kvh0) * (kHeadDim / 8) + (lane & 15)] = v;
-        fence_proxy_async_global();
+        const int64_t row_idx = static_cast<int64_t>(sl) * p.Hkv + kvh0;
+        if constexpr (kFp8) {
+          if (lane < 16) {
+            const bool is_k = lane < 8;
+            const __nv_bfloat16* row = is_k ? p.k_new + b * p.k_new_stride
+                                            : p.v_new + b * p.v_new_stride;
+            const uint4* src = reinterpret_cast<const uint4*>(row + kvh0 * kHeadDim) +
+                               2 * (lane & 7);
+            const uint4 x0 = __ldg(src), x1 = __ldg(src + 1);
+            const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            const float inv = is_k ? p.k_inv : p.v_inv;
+            uint32_t c[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t c0 = e4m3x2_from_f32(bf16lo(w[2 * j]) * inv, bf16hi(w[2 * j]) * inv);
+              const uint32_t c1 =
+                  e4m3x2_from_f32(bf16lo(w[2 * j + 1]) * inv, bf16hi(w[2 * j + 1]) * inv);
+              c[j] = c0 | (c1 << 16);
+            }
+            uint4* pool = is_k ? p.k_pool : p.v_pool;
+            pool[row_idx * (kHeadDim / 16) + (lane & 7)] = make_uint4(c[0], c[1], c[2], c[3]);
+            fence_proxy_async_global();
+          }
+        } else {
+          const __nv_bfloat16* row = lane < 16 ? p.k_new + b * p.k_new_stride
+                                               : p.v_new + b * p.v_new_stride;
+          const uint4 v =
+              __ldg(reinterpret_cast<const uint4*>(row + kvh0 * kHeadDim) + (lane & 15));
+          uint4* pool = lane < 16 ? p.k_pool : p.v_pool;
+          pool[row_idx * (kHeadDim / 8) + (lane & 15)] = v;
+          fence_proxy_async_global();
+        }
       } else if (lane == 0) {
         record_error(p.err, kErrIndex);
       }
@@ -853,6 +882,9 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
   prm.v_new_stride = a.v_new_stride;
   prm.k_pool = static_cast<uint4*>(const_cast<void*>(a.k_cache));
   prm.v_pool = static_cast<uint4*>(const_cast<void*>(a.v_cache));
+  // the store's quantizer multiplies by the binary32 reciprocal of each scale
+  prm.k_inv = 1.0f / a.k_scale;
+  prm.v_inv = 1.0f / a.v_scale;
   prm.prefix_o = nullptr;
   prm.prefix_lse = nullptr;
   if (a.prefix_tokens > 0) {

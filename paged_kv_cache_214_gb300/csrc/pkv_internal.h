@@ -72,7 +72,7 @@ struct DecodeArgs {
   int q_len = 1;      // query positions per sequence (several: speculative verify)
   int fp8 = 0;        // pools hold E4M3 codes: element = code value * k_scale / v_scale
   float k_scale = 1.f, v_scale = 1.f;
-  // Fused store (bf16 pools): before attending, the new token of sequence b
+  // Fused store: before attending, the new token of sequence b
   // (rows of k_new / v_new, token stride in elements) goes to new_slots[b]
   // (-1 = none; otherwise the slot of position context_lens[b] - 1).
   const int32_t* new_slots = nullptr;

@@ -80,6 +80,10 @@ def load_library(path: str = LIB_PATH):
                                                      P, i32, i32, i32, i32, i32, i64, f32, P,
                                                      sz, i32, P]
         lib.paged_decode_attention_store.restype = i32
+        lib.paged_decode_attention_fp8_store.argtypes = [P, P, P, P, P, i64, i64, P, P, P, P,
+                                                         i32, P, i32, i32, i32, i32, i32, i64,
+                                                         f32, f32, f32, P, sz, i32, P]
+        lib.paged_decode_attention_fp8_store.restype = i32
         lib.kv_cache_store_fp8.argtypes = [P, P, i64, i64, P, P, P, i64, i32, i32, i32, i64,
                                            f32, f32, P]
         lib.kv_cache_store_fp8.restype = i32
@@ -346,6 +350,49 @@ def paged_decode_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
         _ptr(context_lens), B, Hq, Hkv, D, bs, NB, float(scale), float(k_scale), float(v_scale),
         _ptr(workspace), ws_bytes, int(num_splits), _stream(stream)),
         "paged_decode_attention_fp8")
+    return out, lse
+
+
+def paged_decode_attention_fp8_store(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                                     slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                                     v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                     context_lens: torch.Tensor, scale: float, k_scale: float,
+                                     v_scale: float, out: Optional[torch.Tensor] = None,
+                                     lse: Optional[torch.Tensor] = None,
+                                     workspace: Optional[torch.Tensor] = None,
+                                     num_splits: int = 0, want_lse: bool = True, stream=None
+                                     ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """kv_cache_store_fp8 of the new tokens (bf16 [B, Hkv, D], slot_mapping[b]
+    -1 or the slot of position context_lens[b] - 1) and the E4M3 decode, in
+    one launch.  Returns (out, lse) as paged_decode_attention_fp8."""
+    lib = load_library()
+    NB, bs, Hkv, D = _fp8_pool_dims(k_cache, v_cache)
+    _need(q, "q", torch.bfloat16, 3)
+    B, Hq, Dq = q.shape
+    if Dq != D:
+        raise ValueError("q head_dim differs from the cache's")
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        _need(t, name, torch.bfloat16, 3, contiguous=False)
+        if tuple(t.shape) != (B, Hkv, D) or t.stride(2) != 1 or t.stride(1) != D:
+            raise ValueError(f"{name} must be [B, {Hkv}, {D}] with contiguous rows")
+    _need(slot_mapping, "slot_mapping", torch.int32, 1)
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    maxblk = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    need = paged_decode_workspace_bytes(B, Hq, Hkv, D, maxblk, bs, num_splits)
+    if workspace is None and need:
+        workspace = decode_workspace(need, q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.paged_decode_attention_fp8_store(
+        _ptr(out), _ptr(lse), _ptr(q), _ptr(k_new), _ptr(v_new), k_new.stride(0),
+        v_new.stride(0), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+        maxblk, _ptr(context_lens), B, Hq, Hkv, D, bs, NB, float(scale), float(k_scale),
+        float(v_scale), _ptr(workspace), ws_bytes, int(num_splits), _stream(stream)),
+        "paged_decode_attention_fp8_store")
     return out, lse
 
 

@@ -207,3 +207,27 @@ def test_decode_b64_workload():
     # the batch-64 decode workload (16 q heads / 8 kv heads, contexts U[512, 4096])
     w = W.config_workload(2, pool_device="cuda")
     run_decode_and_check(w, *SCALES[1], what="decode-b64 fp8")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(16, 8), (32, 8), (64, 8)])
+def test_fused_store_decode_same_bits_as_two_calls(Hq, Hkv):
+    # paged_decode_attention_fp8_store = kv_cache_store_fp8 + the E4M3 decode
+    dev = "cuda"
+    ks, vs = SCALES[1]
+    w = W.make_decode([0, 3, 256, 257, 1000, 3000, 6000], Hq, Hkv, 64, 8700 + Hq)
+    NB, bs = w.num_blocks, w.block_size
+    k8, v8 = store_on_gpu(w.k_cache.view(NB * bs, Hkv, 128), w.v_cache.view(NB * bs, Hkv, 128),
+                          ks, vs, np.arange(NB * bs, dtype=np.int32), NB, Hkv)
+    k8b, v8b = k8.clone(), v8.clone()
+    q, kn, vn, slots = w.q.to(dev), w.k_new.to(dev), w.v_new.to(dev), w.slot_mapping.to(dev)
+    tables, ctx = w.block_tables.to(dev), w.context_lens.to(dev)
+    pkv.kv_cache_store_fp8(kn, vn, k8, v8, slots, ks, vs)
+    o1, l1 = pkv.paged_decode_attention_fp8(q, k8, v8, tables, ctx, w.scale, ks, vs)
+    o2, l2 = pkv.paged_decode_attention_fp8_store(q, kn, vn, slots, k8b, v8b, tables, ctx,
+                                                  w.scale, ks, vs)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == pkv.PKV_OK
+    assert torch.equal(k8, k8b) and torch.equal(v8, v8b)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    # and the oracle agrees with the fused result
+    run_decode_and_check(w, ks, vs, what=f"fused fp8 Hq={Hq}")
