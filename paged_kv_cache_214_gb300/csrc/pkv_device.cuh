@@ -100,13 +100,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Prefetch one box of a 3-D tensor map into L2 (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
-
 // 3-D tiled store of one box from shared memory (bulk async group of the
 // issuing thread).  The shared-memory source must have been fenced for the
 // async proxy (fence_proxy_async_smem) by the threads that wrote it.
@@ -362,8 +355,6 @@ __device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-// Two bf16 in one 32-bit word -> the pair (low element, high element), exact.
-__device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t w) { return pack2(bf16lo(w), bf16hi(w)); }
 
 // D[tmem] (+)= A[tmem] * B[smem]: A (M x K, K-major) read from tensor memory,
 // 16-bit elements packed two per 32-bit column (lower half = lower K index).
