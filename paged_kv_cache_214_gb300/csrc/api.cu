@@ -205,35 +205,73 @@ extern "C" int paged_decode_num_splits(int B, int Hq, int Hkv, int D, int max_bl
   return st ? st : plan.num_splits;
 }
 
+
+
+
+namespace {
+
+// The step's new rows for the fused store (see paged_decode_attention_store).
+struct NewRows {
+  const void* k;
+  const void* v;
+  int64_t k_stride, v_stride;  // elements
+  const int32_t* slots;
+};
+
+// Checks, plan and launch shared by the single-query decode entry points:
+// bf16 or E4M3 pools (a.fp8), with or without the fused store (rows).
+int decode_entry(DecodeArgs a, int D, int block_size, const NewRows* rows,
+                 pkv_stream_t stream) {
+  if (a.B < 0 || a.Hq <= 0 || a.max_blocks_per_seq < 0 || a.num_splits < 0) return PKV_ERR_ARG;
+  if (a.fp8 && (!valid_scale(a.k_scale) || !valid_scale(a.v_scale))) return PKV_ERR_ARG;
+  int st = check_pool(a.Hkv, D, block_size, a.num_blocks);
+  if (st) return st;
+  if (a.Hq % a.Hkv) return PKV_ERR_SHAPE;
+  if (a.B == 0) return PKV_OK;
+  if (!a.out || !a.q || !a.k_cache || !a.v_cache || !a.context_lens) return PKV_ERR_ARG;
+  if (rows && (!rows->k || !rows->v || !rows->slots)) return PKV_ERR_ARG;
+  if (a.max_blocks_per_seq > 0 && !a.block_tables) return PKV_ERR_ARG;
+  if (a.num_blocks == 0 && a.max_blocks_per_seq > 0) return PKV_ERR_ARG;
+  if (!aligned16(a.out) || !aligned16(a.q) || !aligned16(a.k_cache) || !aligned16(a.v_cache))
+    return PKV_ERR_ARG;
+  if (rows) {
+    // new-token rows are read 16 bytes at a time
+    if (!aligned16(rows->k) || !aligned16(rows->v)) return PKV_ERR_ARG;
+    const int64_t row = static_cast<int64_t>(a.Hkv) * D;
+    if (rows->k_stride < row || rows->v_stride < row || rows->k_stride % 8 ||
+        rows->v_stride % 8)
+      return PKV_ERR_ARG;
+    a.new_slots = rows->slots;
+    a.k_new = rows->k;
+    a.v_new = rows->v;
+    a.k_new_stride = rows->k_stride;
+    a.v_new_stride = rows->v_stride;
+  }
+  DecodePlan plan;
+  st = plan_decode(a.B, a.Hq, a.Hkv, a.max_blocks_per_seq, a.num_splits, device_sm_count(), 0,
+                   &plan);
+  if (st) return st;
+  if (plan.workspace_bytes) {
+    if (!a.workspace || a.workspace_bytes < plan.workspace_bytes ||
+        (reinterpret_cast<uintptr_t>(a.workspace) & 255u))
+      return PKV_ERR_WORKSPACE;
+  }
+  unsigned* err = device_error_word();
+  if (!err) return PKV_ERR_LAUNCH;
+  return launch_decode(a, plan, err, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
 extern "C" int paged_decode_attention(void* out, float* lse, const void* q, const void* k_cache,
                                       const void* v_cache, const int32_t* block_tables,
                                       int max_blocks_per_seq, const int32_t* context_lens, int B,
                                       int Hq, int Hkv, int D, int block_size, int64_t num_blocks,
                                       float scale, void* workspace, size_t workspace_bytes,
                                       int num_splits, pkv_stream_t stream) {
-  if (B < 0 || Hq <= 0 || max_blocks_per_seq < 0 || num_splits < 0) return PKV_ERR_ARG;
-  int st = check_pool(Hkv, D, block_size, num_blocks);
-  if (st) return st;
-  if (Hq % Hkv) return PKV_ERR_SHAPE;
-  if (B == 0) return PKV_OK;
-  if (!out || !q || !k_cache || !v_cache || !context_lens) return PKV_ERR_ARG;
-  if (max_blocks_per_seq > 0 && !block_tables) return PKV_ERR_ARG;
-  if (num_blocks == 0 && max_blocks_per_seq > 0) return PKV_ERR_ARG;
-  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
-    return PKV_ERR_ARG;
-  DecodePlan plan;
-  st = plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), 0, &plan);
-  if (st) return st;
-  if (plan.workspace_bytes) {
-    if (!workspace || workspace_bytes < plan.workspace_bytes ||
-        (reinterpret_cast<uintptr_t>(workspace) & 255u))
-      return PKV_ERR_WORKSPACE;
-  }
-  unsigned* err = device_error_word();
-  if (!err) return PKV_ERR_LAUNCH;
   DecodeArgs a{out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                B, Hq, Hkv, num_blocks, scale, workspace, workspace_bytes, num_splits, 0};
-  return launch_decode(a, plan, err, reinterpret_cast<cudaStream_t>(stream));
+  return decode_entry(a, D, block_size, nullptr, stream);
 }
 
 extern "C" int paged_decode_attention_store(
@@ -243,40 +281,24 @@ extern "C" int paged_decode_attention_store(
     const int32_t* context_lens, int B, int Hq, int Hkv, int D, int block_size,
     int64_t num_blocks, float scale, void* workspace, size_t workspace_bytes, int num_splits,
     pkv_stream_t stream) {
-  if (B < 0 || Hq <= 0 || max_blocks_per_seq < 0 || num_splits < 0) return PKV_ERR_ARG;
-  int st = check_pool(Hkv, D, block_size, num_blocks);
-  if (st) return st;
-  if (Hq % Hkv) return PKV_ERR_SHAPE;
-  if (B == 0) return PKV_OK;
-  if (!out || !q || !k_cache || !v_cache || !context_lens || !k_new || !v_new || !slot_mapping)
-    return PKV_ERR_ARG;
-  if (max_blocks_per_seq > 0 && !block_tables) return PKV_ERR_ARG;
-  if (num_blocks == 0 && max_blocks_per_seq > 0) return PKV_ERR_ARG;
-  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
-      !aligned16(k_new) || !aligned16(v_new))
-    return PKV_ERR_ARG;
-  // new-token rows are copied 16 bytes at a time
-  const int64_t row = static_cast<int64_t>(Hkv) * D;
-  if (k_tok_stride < row || v_tok_stride < row || k_tok_stride % 8 || v_tok_stride % 8)
-    return PKV_ERR_ARG;
-  DecodePlan plan;
-  st = plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), 0, &plan);
-  if (st) return st;
-  if (plan.workspace_bytes) {
-    if (!workspace || workspace_bytes < plan.workspace_bytes ||
-        (reinterpret_cast<uintptr_t>(workspace) & 255u))
-      return PKV_ERR_WORKSPACE;
-  }
-  unsigned* err = device_error_word();
-  if (!err) return PKV_ERR_LAUNCH;
   DecodeArgs a{out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                B, Hq, Hkv, num_blocks, scale, workspace, workspace_bytes, num_splits, 0};
-  a.new_slots = slot_mapping;
-  a.k_new = k_new;
-  a.v_new = v_new;
-  a.k_new_stride = k_tok_stride;
-  a.v_new_stride = v_tok_stride;
-  return launch_decode(a, plan, err, reinterpret_cast<cudaStream_t>(stream));
+  const NewRows rows{k_new, v_new, k_tok_stride, v_tok_stride, slot_mapping};
+  return decode_entry(a, D, block_size, &rows, stream);
+}
+
+extern "C" int paged_decode_attention_fp8(void* out, float* lse, const void* q,
+                                          const void* k_cache, const void* v_cache,
+                                          const int32_t* block_tables, int max_blocks_per_seq,
+                                          const int32_t* context_lens, int B, int Hq, int Hkv,
+                                          int D, int block_size, int64_t num_blocks, float scale,
+                                          float k_scale, float v_scale, void* workspace,
+                                          size_t workspace_bytes, int num_splits,
+                                          pkv_stream_t stream) {
+  DecodeArgs a{out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+               B, Hq, Hkv, num_blocks, scale, workspace, workspace_bytes, num_splits, 0, 1,
+               1, k_scale, v_scale};
+  return decode_entry(a, D, block_size, nullptr, stream);
 }
 
 extern "C" int paged_decode_attention_fp8_store(
@@ -286,41 +308,11 @@ extern "C" int paged_decode_attention_fp8_store(
     const int32_t* context_lens, int B, int Hq, int Hkv, int D, int block_size,
     int64_t num_blocks, float scale, float k_scale, float v_scale, void* workspace,
     size_t workspace_bytes, int num_splits, pkv_stream_t stream) {
-  if (B < 0 || Hq <= 0 || max_blocks_per_seq < 0 || num_splits < 0) return PKV_ERR_ARG;
-  if (!valid_scale(k_scale) || !valid_scale(v_scale)) return PKV_ERR_ARG;
-  int st = check_pool(Hkv, D, block_size, num_blocks);
-  if (st) return st;
-  if (Hq % Hkv) return PKV_ERR_SHAPE;
-  if (B == 0) return PKV_OK;
-  if (!out || !q || !k_cache || !v_cache || !context_lens || !k_new || !v_new || !slot_mapping)
-    return PKV_ERR_ARG;
-  if (max_blocks_per_seq > 0 && !block_tables) return PKV_ERR_ARG;
-  if (num_blocks == 0 && max_blocks_per_seq > 0) return PKV_ERR_ARG;
-  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
-      !aligned16(k_new) || !aligned16(v_new))
-    return PKV_ERR_ARG;
-  const int64_t row = static_cast<int64_t>(Hkv) * D;
-  if (k_tok_stride < row || v_tok_stride < row || k_tok_stride % 8 || v_tok_stride % 8)
-    return PKV_ERR_ARG;
-  DecodePlan plan;
-  st = plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), 0, &plan);
-  if (st) return st;
-  if (plan.workspace_bytes) {
-    if (!workspace || workspace_bytes < plan.workspace_bytes ||
-        (reinterpret_cast<uintptr_t>(workspace) & 255u))
-      return PKV_ERR_WORKSPACE;
-  }
-  unsigned* err = device_error_word();
-  if (!err) return PKV_ERR_LAUNCH;
   DecodeArgs a{out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                B, Hq, Hkv, num_blocks, scale, workspace, workspace_bytes, num_splits, 0, 1,
                1, k_scale, v_scale};
-  a.new_slots = slot_mapping;
-  a.k_new = k_new;
-  a.v_new = v_new;
-  a.k_new_stride = k_tok_stride;
-  a.v_new_stride = v_tok_stride;
-  return launch_decode(a, plan, err, reinterpret_cast<cudaStream_t>(stream));
+  const NewRows rows{k_new, v_new, k_tok_stride, v_tok_stride, slot_mapping};
+  return decode_entry(a, D, block_size, &rows, stream);
 }
 
 // Longest run of query positions per sequence the multi-query decode accepts.
@@ -390,40 +382,6 @@ extern "C" int paged_decode_attention_multiquery(
   return launch_decode(a, plan, err, reinterpret_cast<cudaStream_t>(stream));
 }
 
-extern "C" int paged_decode_attention_fp8(void* out, float* lse, const void* q,
-                                          const void* k_cache, const void* v_cache,
-                                          const int32_t* block_tables, int max_blocks_per_seq,
-                                          const int32_t* context_lens, int B, int Hq, int Hkv,
-                                          int D, int block_size, int64_t num_blocks, float scale,
-                                          float k_scale, float v_scale, void* workspace,
-                                          size_t workspace_bytes, int num_splits,
-                                          pkv_stream_t stream) {
-  if (B < 0 || Hq <= 0 || max_blocks_per_seq < 0 || num_splits < 0) return PKV_ERR_ARG;
-  if (!valid_scale(k_scale) || !valid_scale(v_scale)) return PKV_ERR_ARG;
-  int st = check_pool(Hkv, D, block_size, num_blocks);
-  if (st) return st;
-  if (Hq % Hkv) return PKV_ERR_SHAPE;
-  if (B == 0) return PKV_OK;
-  if (!out || !q || !k_cache || !v_cache || !context_lens) return PKV_ERR_ARG;
-  if (max_blocks_per_seq > 0 && !block_tables) return PKV_ERR_ARG;
-  if (num_blocks == 0 && max_blocks_per_seq > 0) return PKV_ERR_ARG;
-  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
-    return PKV_ERR_ARG;
-  DecodePlan plan;
-  st = plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), 0, &plan);
-  if (st) return st;
-  if (plan.workspace_bytes) {
-    if (!workspace || workspace_bytes < plan.workspace_bytes ||
-        (reinterpret_cast<uintptr_t>(workspace) & 255u))
-      return PKV_ERR_WORKSPACE;
-  }
-  unsigned* err = device_error_word();
-  if (!err) return PKV_ERR_LAUNCH;
-  DecodeArgs a{out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-               B, Hq, Hkv, num_blocks, scale, workspace, workspace_bytes, num_splits, 0, 1,
-               1, k_scale, v_scale};
-  return launch_decode(a, plan, err, reinterpret_cast<cudaStream_t>(stream));
-}
 
 namespace {
 
