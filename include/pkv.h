@@ -11,6 +11,19 @@
  *                            cached prefix plus the new tokens, all read through
  *                            block_tables
  *
+ * and, built on them:
+ *   paged_decode_attention_store      a decode step's store and decode in one
+ *                                     launch
+ *   paged_decode_attention_shared_prefix  decode with a prefix that every
+ *                                     sequence shares attended once per kv head
+ *   paged_decode_attention_multiquery several new positions per sequence (the
+ *                                     verify step of speculative decoding)
+ *   kv_cache_store_fp8, paged_decode_attention_fp8(_store)  the same over E4M3
+ *                                     (FP8) pools
+ *   kv_cache_copy_blocks              copy-on-write block copies
+ *   paged_decode_attention_noalloc    decode without a caller workspace
+ * (the host block manager is declared in pkv_blocks.h).
+ *
  * Conventions shared by every call
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
  *     never allocates, frees or retains them.  Sizes are element counts.
