@@ -696,26 +696,39 @@ def run_fp8_extra(pkv, dev, hbm_peak, flush, stream, cfg):
     def call():
         pkv.paged_decode_attention_fp8(q, k8, v8, tables, lens, w.scale, ks, vs, out=out,
                                        lse=lse, workspace=ws, stream=stream)
-    for _ in range(10):
-        call()
-    times = []
-    for _ in range(50):
-        _flush_l2(flush)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        call()
-        b.record(stream)
-        times.append((a, b))
-    torch.cuda.synchronize()
-    ms = sorted(x.elapsed_time(y) for x, y in times)
-    med = ms[len(ms) // 2]
+    kn, vn, slots = w.k_new.to(dev), w.v_new.to(dev), w.slot_mapping.to(dev)
+
+    def fused():
+        pkv.paged_decode_attention_fp8_store(q, kn, vn, slots, k8, v8, tables, lens, w.scale,
+                                             ks, vs, out=out, lse=lse, workspace=ws,
+                                             stream=stream)
+
+    def median_us(fn):
+        for _ in range(10):
+            fn()
+        times = []
+        for _ in range(50):
+            _flush_l2(flush)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            times.append((a, b))
+        torch.cuda.synchronize()
+        ms = sorted(x.elapsed_time(y) for x, y in times)
+        return ms[len(ms) // 2], ms[0]
+    med, mn = median_us(call)
+    med_f, _ = median_us(fused)
     gbs = decode_bytes(w, kv_elem_bytes=1) / (med / 1e3) / 1e9
     entry = {"workload": w.name + "-fp8", "median_us": round(med * 1e3, 2),
-             "min_us": round(ms[0] * 1e3, 2), "kv_tokens": w.kv_tokens,
+             "min_us": round(mn * 1e3, 2), "kv_tokens": w.kv_tokens,
              "kv_tokens_per_s": round(w.kv_tokens / (med / 1e3), 1), "GB/s": round(gbs, 1),
              "frac_of_peak": round(gbs / hbm_peak, 4),
-             "note": "E4M3 K/V, one byte per element (GB/s counts those bytes)"}
-    del w, q, k8, v8, tables, lens, out, lse, ws
+             "fused_store_step_us": round(med_f * 1e3, 2),
+             "note": "E4M3 K/V, one byte per element (GB/s counts those bytes); "
+                     "fused_store_step_us: the step's store of the new tokens and the "
+                     "decode as one launch (paged_decode_attention_fp8_store)"}
+    del w, q, k8, v8, tables, lens, out, lse, ws, kn, vn, slots
     torch.cuda.empty_cache()
     return entry
 
