@@ -12,7 +12,8 @@ consecutive steps cycle through three batches whose blocks are disjoint, so no
 step finds the previous step's K/V in L2.
 
 Prints one JSON line (rank 0).  `value` is algorithmic HBM bytes per step
-(store + decode, see DESIGN notes) x steps / device time, in GB/s; the same line
+(the decode's 4096 B per context token plus q, out, lse and table entries, and
+the store's new rows read and written) x steps / device time, in GB/s; the same line
 carries KV-tokens/s, the roofline of the step's kernel, the oracle
 timed on the host cores (`cpu_baseline`), an end-to-end number through the
 public API with host buffers (`e2e`), clocks sampled during the timed region
