@@ -88,8 +88,8 @@ struct DecodeParams {
   int prefix_splits;        // partials per row of the shared-prefix pass
   const float* prefix_o;    // [B*Hq, prefix_splits, 128]
   const float* prefix_lse;  // [B*Hq, prefix_splits] log2-sum-exp
-  // Fused store (bf16 pools; new_slots == nullptr: none): the new token of
-  // sequence b, rows k_new / v_new + b * stride, goes to slot new_slots[b].
+  // Fused store (new_slots == nullptr: none): the new token of sequence b,
+  // bf16 rows k_new / v_new + b * stride, goes to slot new_slots[b].
   const int32_t* new_slots;
   const __nv_bfloat16* k_new;
   const __nv_bfloat16* v_new;
@@ -295,12 +295,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   const int tok_end = min(ctx, tok_begin + split_tokens);
   const int n_tiles = (tok_end - tok_begin + kTile - 1) / kTile;
 
-  // Every warp is a producer for one quarter of each stage (warp w loads
-  // K dims [0,64), K [64,128), V [0,64), V [64,128) for w = 0..3): one thread
-  // streams its tensor copies one after another at a few hundred cycles each,
-  // so four issuing threads land a stage sooner than one.  Lane 0 of each warp
-  // fills its quarter of the ring up front and refills it as soon as all four
-  // warps have released the stage.
+  // bf16: every warp is a producer for one quarter of each stage (warp w
+  // loads K dims [0,64), K [64,128), V [0,64), V [64,128) for w = 0..3): one
+  // thread streams its tensor copies one after another at a few hundred cycles
+  // each, so four issuing threads land a stage sooner than one.  E4M3: warps 0
+  // and 1 copy the stage's K and V box.  Lane 0 of each issuing warp fills its
+  // part of the ring up front and refills the stage released one tile earlier.
   const uint64_t policy = l2_policy_evict_first();
   auto issue = [&](int it) {
     const int s = it % kStagesN;
