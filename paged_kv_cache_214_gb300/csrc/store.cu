@@ -1,4 +1,5 @@
-// store.cu — kv_cache_store for sm_103a.
+// store.cu — kv_cache_store, kv_cache_store_fp8 and kv_cache_copy_blocks for
+// sm_103a.
 //
 // Operation: new K/V rows are written into the paged cache through slot_mapping
 // ("Nano-vLLM System Architecture Analysis", §2 Core Components, "Attention with
@@ -9,7 +10,11 @@
 // Design: a plain bandwidth kernel.  Consecutive threads move consecutive
 // 16-byte pieces of the same row (coalesced reads and writes); the grid is a
 // multiple of the SM count and strides over (token, K|V, piece).  Padding slots
-// (< 0) are skipped; out-of-range slots are skipped and reported.
+// (< 0) are skipped; out-of-range slots are skipped and reported.  The E4M3
+// variant converts each 16-element piece to one-byte codes on the way (the
+// quantized KV cache that "Why Understand Inference Engine Architecture?",
+// Tensor Parallelism Optimization, names); the block copy serves
+// copy-on-write ("Paged KV Cache", reference counting).
 
 #include <cuda_bf16.h>
 
