@@ -130,6 +130,23 @@ def test_decode_store_host_checks(lib):
               None, 0, 0, s) == pkv.PKV_ERR_ARG
 
 
+def test_fp8_decode_store_host_checks(lib):
+    s = None
+    ds = lib.paged_decode_attention_fp8_store
+    P = 16  # a stand-in device address: the checks below fail before any use
+    nan = float("nan")
+    # scales are checked first, then as paged_decode_attention_store
+    for ks, vs in ((0.0, 1.0), (1.0, -2.0), (nan, 1.0), (1.0, float("inf"))):
+        assert ds(P, None, P, P, P, 1024, 1024, P, P, P, P, 1, P, 2, 16, 8, 128, 256, 4, 1.0,
+                  ks, vs, None, 0, 0, s) == pkv.PKV_ERR_ARG
+    assert ds(None, None, None, None, None, 1024, 1024, None, None, None, None, 1, None, 0, 16,
+              8, 128, 256, 4, 1.0, 0.5, 0.5, None, 0, 0, s) == pkv.PKV_OK
+    assert ds(None, None, None, None, None, 1024, 1024, None, None, None, None, 1, None, 2, 16,
+              8, 128, 256, 4, 1.0, 0.5, 0.5, None, 0, 0, s) == pkv.PKV_ERR_ARG
+    assert ds(P, None, P, P, P, 1020, 1024, P, P, P, P, 1, P, 2, 16, 8, 128, 256, 4, 1.0, 0.5,
+              0.5, None, 0, 0, s) == pkv.PKV_ERR_ARG
+
+
 def test_workspace_query_and_split_plan(lib):
     # one split needs no workspace; several need partials + counters
     assert pkv.paged_decode_workspace_bytes(4, 16, 8, 128, 1, 256, 1) == 0
