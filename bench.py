@@ -119,7 +119,13 @@ class ClockSampler:
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
-        time.sleep(0.15)
+        # nvidia-smi's start-up (library load, device attach) must not overlap
+        # the timed region: wait (at most 5 s) for its first sample
+        t0 = time.perf_counter()
+        while self.proc is not None and time.perf_counter() - t0 < 5.0:
+            if self.proc.poll() is not None or os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.01)
 
     def stop(self):
         if self.proc is None:
@@ -326,16 +332,16 @@ def run_gpu(args, world, rank):
     dev_inputs = (q, kn, vn, kc, vc, tables, slots, lens)
 
     step_bytes = store_bytes(w.B, w.Hkv, w.D) + decode_bytes(w)
-    dec_bytes = decode_bytes(w)
 
+    # The clock sampler starts before the warm-up, so that the warm-up steps
+    # run right before the timed region and the GPU does not sit idle first.
+    clocks = ClockSampler(dev.index)
+    if rank == 0:
+        clocks.start()
     for i in range(args.warmup):
         _decode_step(pkv, w, dev_inputs, i % R, ws, out, lse, stream)
     torch.cuda.synchronize()
     assert pkv.get_device_error() == pkv.PKV_OK
-
-    clocks = ClockSampler(dev.index)
-    if rank == 0:
-        clocks.start()
     K = args.steps
     # A step is one launch (store + decode), so the launches run back to back
     # and their average duration is the timed region over K: no event sits
@@ -378,11 +384,7 @@ def run_gpu(args, world, rank):
         "steps": K, "warmup": args.warmup, "ms_per_step": round(elapsed_ms / K, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16, shuffled 2048-block pool)",
-        "config": {"workload": WORKLOAD, "global_batch": w.B * world,
-                   "kv_tokens_per_step": w.kv_tokens, "store_tokens_per_step": w.B,
-                   "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2: {dec_bytes / 1e6:.0f} MB K/V per step, "
-                         f"{R} rotating batches with disjoint blocks"},
+        "config": bench_config(w, world, R),
         "kv_tokens_per_s": round(kv_tps, 1),
         "pct_of_peak_hbm": round(100 * value / hbm_peak, 2),
         "gpu_launches": K,
@@ -409,6 +411,16 @@ def run_gpu(args, world, rank):
             result["cpu_baseline"] = time_oracle(W.config_workload(2, pool_device=dev))
             result["cpu_baseline"]["single_core"] = time_oracle_single_core(dev)
     return result
+
+
+def bench_config(w, world, rotations=ROTATIONS):
+    """The workload description both arms print (the same dict for the same
+    workload)."""
+    return {"workload": WORKLOAD, "global_batch": w.B * world,
+            "kv_tokens_per_step": w.kv_tokens, "store_tokens_per_step": w.B,
+            "parallelism": f"replicas x{world}",
+            "l2": f"inputs larger than L2: {decode_bytes(w) / 1e6:.0f} MB K/V per step, "
+                  f"{rotations} rotating batches with disjoint blocks"}
 
 
 def _trimmed_decode_b64(dev):
@@ -836,7 +848,7 @@ def run_reference(args, world, rank):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el * 1e3 / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "global_batch": w.B, "parallelism": "host cores"},
+        "config": bench_config(w, world),
         "kv_tokens_per_s": round(s["tokens"] * args.steps / el, 1),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle", "sample": sample},

@@ -256,7 +256,11 @@ int paged_decode_attention_shared_prefix(void* out, float* lse, const void* q,
  *     returns PKV_ERR_WORKSPACE and launches nothing.
  *   - The first call on a device looks up the array's device address once
  *     (cudaGetSymbolAddress) and caches it; make that first call before any
- *     stream capture starts on that device.
+ *     stream capture starts on that device.  The cached address belongs to
+ *     the device's context at that time: after cudaDeviceReset on a device,
+ *     do not call this entry point on that device again in the same process.
+ *   - Argument checks run before anything is queued: a call refused with any
+ *     status launches nothing and queues nothing on `stream`.
  *   - Every call on a device uses the same array, which keeps the previous
  *     call's contents; each call clears its own arrival counters (an async
  *     memset on `stream`) before its kernel.  Calls whose work overlaps on the

@@ -218,10 +218,9 @@ struct NewRows {
   const int32_t* slots;
 };
 
-// Checks, plan and launch shared by the single-query decode entry points:
-// bf16 or E4M3 pools (a.fp8), with or without the fused store (rows).
-int decode_entry(DecodeArgs a, int D, int block_size, const NewRows* rows,
-                 pkv_stream_t stream) {
+}  // namespace
+
+int pkv::check_decode_args(const DecodeArgs& a, int D, int block_size) {
   if (a.B < 0 || a.Hq <= 0 || a.max_blocks_per_seq < 0 || a.num_splits < 0) return PKV_ERR_ARG;
   if (a.fp8 && (!valid_scale(a.k_scale) || !valid_scale(a.v_scale))) return PKV_ERR_ARG;
   int st = check_pool(a.Hkv, D, block_size, a.num_blocks);
@@ -229,11 +228,22 @@ int decode_entry(DecodeArgs a, int D, int block_size, const NewRows* rows,
   if (a.Hq % a.Hkv) return PKV_ERR_SHAPE;
   if (a.B == 0) return PKV_OK;
   if (!a.out || !a.q || !a.k_cache || !a.v_cache || !a.context_lens) return PKV_ERR_ARG;
-  if (rows && (!rows->k || !rows->v || !rows->slots)) return PKV_ERR_ARG;
   if (a.max_blocks_per_seq > 0 && !a.block_tables) return PKV_ERR_ARG;
   if (a.num_blocks == 0 && a.max_blocks_per_seq > 0) return PKV_ERR_ARG;
   if (!aligned16(a.out) || !aligned16(a.q) || !aligned16(a.k_cache) || !aligned16(a.v_cache))
     return PKV_ERR_ARG;
+  return PKV_OK;
+}
+
+namespace {
+
+// Checks, plan and launch shared by the single-query decode entry points:
+// bf16 or E4M3 pools (a.fp8), with or without the fused store (rows).
+int decode_entry(DecodeArgs a, int D, int block_size, const NewRows* rows,
+                 pkv_stream_t stream) {
+  int st = check_decode_args(a, D, block_size);
+  if (st || a.B == 0) return st;
+  if (rows && (!rows->k || !rows->v || !rows->slots)) return PKV_ERR_ARG;
   if (rows) {
     // new-token rows are read 16 bytes at a time
     if (!aligned16(rows->k) || !aligned16(rows->v)) return PKV_ERR_ARG;

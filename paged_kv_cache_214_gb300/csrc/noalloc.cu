@@ -12,7 +12,9 @@
 // The array is a device symbol.  Host code cannot use its name as an address
 // (on the host the name is only a stand-in), so the device address is looked up
 // with cudaGetSymbolAddress once per device, the first time the entry point is
-// called on that device, and cached.
+// called on that device, and cached.  The cached address belongs to the
+// device's current context: after cudaDeviceReset on a device this entry
+// point must not be called on that device again in the same process.
 
 #include <cuda_runtime.h>
 
@@ -61,11 +63,15 @@ extern "C" int paged_decode_attention_noalloc(void* out, float* lse, const void*
                                               int Hkv, int D, int block_size,
                                               int64_t num_blocks, float scale, int num_splits,
                                               pkv_stream_t stream) {
-  if (D != kHeadDim || block_size != kBlockSize) return PKV_ERR_SHAPE;
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || max_blocks_per_seq < 0 || num_splits < 0)
-    return PKV_ERR_ARG;
+  // Every argument check of the decode call runs first: a refused call
+  // queues nothing on the stream (not even the counter clear below).
+  const DecodeArgs args{out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                        context_lens, B, Hq, Hkv, num_blocks, scale, nullptr, 0,
+                        num_splits, 0};
+  int st = check_decode_args(args, D, block_size);
+  if (st || B == 0) return st;
   DecodePlan plan;
-  int st = plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), 0, &plan);
+  st = plan_decode(B, Hq, Hkv, max_blocks_per_seq, num_splits, device_sm_count(), 0, &plan);
   if (st) return st;
   // This call's partials and counters must fit the fixed scratch array.
   if (plan.workspace_bytes > kNoAllocScratchBytes) return PKV_ERR_WORKSPACE;

@@ -81,6 +81,11 @@ struct DecodeArgs {
   int64_t k_new_stride = 0, v_new_stride = 0;
 };
 
+// Argument checks of a single-query decode call (pointers, alignment, pool
+// shape, head grouping); PKV_OK or the status the call returns.  Launches
+// nothing.
+int check_decode_args(const DecodeArgs& a, int D, int block_size);
+
 // Split plan of one decode call.
 struct DecodePlan {
   int heads_per_cta;  // G: query heads per kv head that one thread block serves
