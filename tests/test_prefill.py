@@ -1,5 +1,7 @@
 """paged_prefill_attention (tcgen05) on the GPU against the oracle, after the
 store of the chunk's new tokens (max|dout| <= 1e-2, max|dlse| <= 1e-3)."""
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -69,13 +71,25 @@ def test_no_prefix_long_prompt():
     run_and_check(w, what="no prefix")
 
 
-def test_chunked_prefill_b16_sampled():
+def test_chunked_prefill_b16_full():
+    """Every row and head of the chunked-prefill workload (16 sequences)."""
     w = W.config_workload(4, pool_device="cuda")
-    run_and_check(w, sample=[0, 9, 15], what="chunked-prefill-b16")
+    t0 = time.perf_counter()
+    run_and_check(w, what="chunked-prefill-b16")
+    print(f"chunked-prefill-b16: GPU + oracle check of all {w.B} sequences "
+          f"{time.perf_counter() - t0:.1f} s")
 
 
-def test_lk_less_than_lq_is_reported():
-    w = W.make_prefill([0, 100], [64, 64], 8, 8, 8, 5400)
+@pytest.mark.parametrize("Hq,Hkv", [(2, 1), (16, 8), (6, 1)])
+def test_no_prefix_even_groups(Hq, Hkv):
+    # two query heads per item (even group sizes), prompts with no cached prefix
+    w = W.make_prefill([0, 0, 0], [1000, 128, 77], Hq, Hkv, 32, 5310 + Hq)
+    run_and_check(w, what=f"no prefix Hq={Hq} Hkv={Hkv}")
+
+
+@pytest.mark.parametrize("Hq", [8, 16])
+def test_lk_less_than_lq_is_reported(Hq):
+    w = W.make_prefill([0, 100], [64, 64], Hq, 8, 8, 5400)
     dev = "cuda"
     cu_k = w.cu_seqlens_k.clone()
     cu_k[2] = cu_k[1] + 10            # sequence 1: Lk = 10 < Lq = 64
@@ -87,8 +101,9 @@ def test_lk_less_than_lq_is_reported():
     assert pkv.get_device_error() == pkv.PKV_OK
 
 
-def test_bad_block_id_is_reported():
-    w = W.make_prefill([300], [64], 8, 8, 8, 5500)
+@pytest.mark.parametrize("Hq", [8, 16])
+def test_bad_block_id_is_reported(Hq):
+    w = W.make_prefill([300], [64], Hq, 8, 8, 5500)
     dev = "cuda"
     bt = w.block_tables.clone()
     bt[0, 0] = -3
