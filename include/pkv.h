@@ -22,6 +22,7 @@
  *                                     (FP8) pools
  *   kv_cache_copy_blocks              copy-on-write block copies
  *   paged_decode_attention_noalloc    decode without a caller workspace
+ *   pkv_testing_set_wait_fault        tests only: make a bounded wait run out
  * (the host block manager is declared in pkv_blocks.h).
  *
  * Conventions shared by every call
@@ -393,6 +394,29 @@ int pkv_get_device_error(pkv_stream_t stream);
 
 /* pkv_status_string — static, human-readable name of a status code. */
 const char* pkv_status_string(int status);
+
+/* pkv_testing_set_wait_fault — FOR TESTS ONLY: exercises the bounded-wait
+ * failure path of the kernels without faulting or hanging the GPU.  The pages
+ * have no counterpart; every mbarrier wait of this library's kernels is
+ * bounded (PKV_ERR_TIMEOUT, then the block waits for its own copies in flight,
+ * frees its tensor memory and exits), and this call lets a test make such a
+ * wait run out.
+ *   wait_limit_ns > 0 : the kernels' wait limit becomes this many ns (at most
+ *                       2e9, the built-in limit); 0 restores the built-in limit.
+ *   withhold_tile >= 0: the K/V copy producers of paged_decode_attention (and
+ *                       its fused / E4M3 / multi-query forms on the split-K
+ *                       kernel) stop before that tile of each block's key range
+ *                       (64-token tiles), and those of the tensor-core kernel
+ *                       (prefill, shared-prefix pass, verify) before that
+ *                       128-key tile of each block's running count, so that a
+ *                       consumer's wait on it runs out while no copy is
+ *                       outstanding on its barrier; -1: copy everything.  Needs
+ *                       wait_limit_ns > 0.
+ * The setting is per process, applies to every later launch on the current
+ * device until changed, and is set synchronously (cudaMemcpyToSymbol).  Call
+ * pkv_testing_set_wait_fault(0, -1) to turn it off.  Returns PKV_OK,
+ * PKV_ERR_ARG or PKV_ERR_LAUNCH. */
+int pkv_testing_set_wait_fault(int64_t wait_limit_ns, int withhold_tile);
 
 #ifdef __cplusplus
 }

@@ -15,6 +15,8 @@ namespace pkv {
 namespace {
 
 constexpr int kMaxDevices = 64;
+// Longest wait limit the test hook accepts (the kernels' own limit).
+constexpr unsigned long long kWaitLimitTestMaxNs = 2000000000ull;
 
 // The one piece of state the library keeps: a sticky error word per device,
 // or-ed by kernels and read-and-cleared by pkv_get_device_error().
@@ -504,6 +506,17 @@ extern "C" int pkv_get_device_error(pkv_stream_t stream) {
   if (v & kErrIndex) return PKV_ERR_DEVICE_INDEX;
   if (v & kErrTimeout) return PKV_ERR_TIMEOUT;
   return PKV_OK;
+}
+
+extern "C" int pkv_testing_set_wait_fault(int64_t wait_limit_ns, int withhold_tile) {
+  if (wait_limit_ns < 0 || withhold_tile < -1 || (withhold_tile >= 0 && wait_limit_ns == 0) ||
+      wait_limit_ns > static_cast<int64_t>(kWaitLimitTestMaxNs))
+    return PKV_ERR_ARG;
+  const unsigned long long lim = static_cast<unsigned long long>(wait_limit_ns);
+  const int w = withhold_tile + 1;
+  int st = set_wait_hook_decode(lim, w);
+  if (st == PKV_OK) st = set_wait_hook_prefill(lim, w);
+  return st;
 }
 
 extern "C" const char* pkv_status_string(int status) {

@@ -302,7 +302,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   // and 1 copy the stage's K and V box.  Lane 0 of each issuing warp fills its
   // part of the ring up front and refills the stage released one tile earlier.
   const uint64_t policy = l2_policy_evict_first();
+  const int withhold = withheld_tile();   // test hook: tiles from here on are never copied
   auto issue = [&](int it) {
+    if (it >= withhold) return;
     const int s = it % kStagesN;
     const int tok = tok_begin + it * kTile;
     const int slot = sblk[tok / kBlockSize - blk_begin] * kBlockSize + tok % kBlockSize;
@@ -768,6 +770,11 @@ int launch_g(const DecodeArgs& a, const DecodePlan& plan, const DecodeParams& pr
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
+
+int set_wait_hook_decode(unsigned long long limit_ns, int withhold_plus1) {
+  const WaitHook h{limit_ns, withhold_plus1, 0};
+  return cudaMemcpyToSymbol(g_wait_hook, &h, sizeof h) == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+}
 
 int plan_decode(int B, int Hq, int Hkv, int max_blocks_per_seq, int num_splits,
                 int sm_count, int prefix_blocks, DecodePlan* plan) {

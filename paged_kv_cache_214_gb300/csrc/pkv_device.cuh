@@ -15,6 +15,19 @@ namespace pkv {
 // never complete, and the kernel gives up rather than hanging the device.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
+// Test hook (all zero: off).  limit_ns, when not 0, replaces the wait limit;
+// withhold_plus1 = k + 1 makes the K/V copy producers of the decode and
+// prefill kernels stop before tile k of their range (decode: tile of the
+// block's key range, prefill: the CTA's running K tile count), so that a
+// consumer's wait on it runs out while no copy is outstanding on its barrier.
+// One copy per translation unit; set through pkv_testing_set_wait_fault() only.
+struct WaitHook {
+  unsigned long long limit_ns;
+  int withhold_plus1;
+  int unused;
+};
+static __device__ WaitHook g_wait_hook;
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -66,10 +79,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
+  const unsigned long long hook = __ldcg(&g_wait_hook.limit_ns);
+  const uint64_t limit = hook ? hook : kWaitLimitNs;
   while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit) return false;
   }
   return true;
+}
+
+// First tile a producer must not copy (the test hook's withheld tile; a
+// large value when the hook is off).
+__device__ __forceinline__ int withheld_tile() {
+  const int w = __ldcg(&g_wait_hook.withhold_plus1);
+  return w > 0 ? w - 1 : INT32_MAX;
 }
 
 // ---------------------------------------------------------------- TMA

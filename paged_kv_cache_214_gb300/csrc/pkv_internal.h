@@ -160,6 +160,11 @@ struct VerifyArgs {
   float scale;
 };
 int verify_rows_fit(int g, int q_len);
+
+// Test hook of the decode / prefill kernels' bounded waits (see
+// pkv_testing_set_wait_fault); 0, 0 turns it off.
+int set_wait_hook_decode(unsigned long long limit_ns, int withhold_plus1);
+int set_wait_hook_prefill(unsigned long long limit_ns, int withhold_plus1);
 int launch_verify(const VerifyArgs& a, unsigned* err, cudaStream_t stream);
 
 }  // namespace pkv

@@ -336,10 +336,11 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
     // ------------------------------------------------------------ TMA: Q and K
     // An item's Q goes into the single Q buffer right after its first K tile
     // has been issued, once the S MMAs of the previous item are done with it.
-    bool ok = true;
+    bool ok = true, stopped = false;
     int gi = 0, gk = 0;
     BlockIds ids;
     Ring<kKStages> rk;
+    const int withhold = withheld_tile();   // test hook: K tiles from here on are never copied
     auto load_q = [&](const Item& it, int qi) -> bool {
       const uint32_t qdst = sbase + kOffQ;
       if (qi >= 1 && !warp_wait(bar(kBarQEmpty), (qi - 1) & 1)) return false;
@@ -391,6 +392,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
       ids.chunk = -1;
       for (int kt = 0; kt < it.n; ++kt, ++gk, rk.next()) {
         if (__any_sync(kFull, flags[0] != 0)) { ok = false; break; }
+        if (gk >= withhold) { stopped = true; break; }
         const int gkt = it.kt0 + kt;
         const int id = ids.get(it.table, table_limit, gkt >> 1, lane, p.num_blocks, p.err);
         const int slot = id * kBlockSize + (gkt & 1) * kN;
@@ -416,7 +418,7 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
           break;
         }
       }
-      if (!ok) break;
+      if (!ok || stopped) break;
       ++gi;
       it = nx;
       k = k2;
@@ -828,6 +830,11 @@ int grid_for(int n_items) {
 }
 
 }  // namespace
+
+int set_wait_hook_prefill(unsigned long long limit_ns, int withhold_plus1) {
+  const WaitHook h{limit_ns, withhold_plus1, 0};
+  return cudaMemcpyToSymbol(g_wait_hook, &h, sizeof h) == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
+}
 
 int prefix_rows_per_tile(int g) { return (g >= 1 && g <= kM) ? (kM / g) * g : 0; }
 

@@ -97,6 +97,8 @@ def load_library(path: str = LIB_PATH):
         lib.pkv_get_device_error.restype = i32
         lib.pkv_status_string.argtypes = [i32]
         lib.pkv_status_string.restype = ctypes.c_char_p
+        lib.pkv_testing_set_wait_fault.argtypes = [i64, i32]
+        lib.pkv_testing_set_wait_fault.restype = i32
         _lib = lib
         return lib
 
@@ -554,6 +556,14 @@ def paged_prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
                                        int(max_seqlen_k), Hq, Hkv, D, bs, NB, float(scale),
                                        _stream(stream)), "paged_prefill_attention")
     return out, lse
+
+
+def testing_set_wait_fault(wait_limit_ns: int, withhold_tile: int = -1) -> None:
+    """For tests only: lower the kernels' wait limit and make the copy
+    producers withhold one tile (see pkv_testing_set_wait_fault in pkv.h);
+    testing_set_wait_fault(0, -1) turns it off."""
+    _check(load_library().pkv_testing_set_wait_fault(int(wait_limit_ns), int(withhold_tile)),
+           "pkv_testing_set_wait_fault")
 
 
 def get_device_error(stream=None) -> int:
