@@ -75,7 +75,7 @@ struct DecodeParams {
   // Hq counts "virtual" heads: q_len query positions x the physical heads;
   // virtual head v of kv head kv is position (v%g)/(g/q_len), head
   // kv*(g/q_len) + (v%g)%(g/q_len), with g = Hq/Hkv.  q_len = 1 is plain decode.
-  int B, Hq, Hkv, maxblk, num_splits, split_blocks, head_groups;
+  int B, Hq, Hkv, maxblk, num_splits, split_tokens, head_groups;
   int q_len, Hq_phys;
   float k_scale, v_scale;   // FP8 pools: element value = code value * scale
   int64_t num_blocks;
@@ -227,11 +227,15 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   const int lane = tid & 31;
 
   // Block ids of this split's whole range, loaded speculatively (they do not
-  // depend on the context length, so both loads are in flight together).
-  const int split_tokens = p.split_blocks * kBlockSize;
+  // depend on the context length, so both loads are in flight together).  A
+  // range is whole blocks, or (small batches) whole 64-token tiles, which may
+  // start inside a block and so touch one block more.
+  const int split_tokens = p.split_tokens;
   const int blk_begin = (p.prefix_tokens + split * split_tokens) / kBlockSize;
+  const int range_blocks = split_tokens % kBlockSize == 0 ? split_tokens / kBlockSize
+                                                          : split_tokens / kBlockSize + 2;
   int spec_id = 0;
-  if (warp == 0 && lane < p.split_blocks && blk_begin + lane < p.maxblk)
+  if (warp == 0 && lane < range_blocks && blk_begin + lane < p.maxblk)
     spec_id = __ldg(p.block_tables + static_cast<int64_t>(b) * p.maxblk + blk_begin + lane);
   // Context of this sequence (clamped to what its block table can address).
   int ctx = p.context_lens[b];
@@ -792,15 +796,22 @@ int plan_decode(int B, int Hq, int Hkv, int max_blocks_per_seq, int num_splits,
   const int kv_groups = Hkv;
   const int rest = max_blocks_per_seq - prefix_blocks;
   const int maxblk = rest > 0 ? rest : 1;
+  const int sms = sm_count > 0 ? sm_count : 148;
+  const int64_t seq_units = static_cast<int64_t>(B) * kv_groups * plan->head_groups;
   int split_blocks;
+  bool small = false;
   if (num_splits > 0) {
     split_blocks = (maxblk + num_splits - 1) / num_splits;
   } else {
     // Enough (sequence, head group, split) units for about eight waves of two
     // blocks per SM if every context were full length; whole blocks per split.
-    const int64_t units = static_cast<int64_t>(B) * kv_groups * plan->head_groups * maxblk;
-    const int64_t target = static_cast<int64_t>(sm_count > 0 ? sm_count : 148) * 2 * 8;
+    const int64_t units = seq_units * maxblk;
+    const int64_t target = static_cast<int64_t>(sms) * 2 * 8;
     split_blocks = static_cast<int>((units + target - 1) / target);
+    // A batch whose one-block splits would not even fill one wave of one
+    // block per SM splits into 64-token tiles instead (a launch-latency
+    // bound step: more blocks, each with a shorter chain of copies).
+    small = units < sms;
     if (split_blocks < 2) split_blocks = maxblk < 2 ? maxblk : 2;
   }
   if (split_blocks < 1) split_blocks = 1;
@@ -809,7 +820,18 @@ int plan_decode(int B, int Hq, int Hkv, int max_blocks_per_seq, int num_splits,
   if (S > kMaxSplits) return PKV_ERR_SHAPE;
   // re-balance so that the splits are as even as possible
   split_blocks = (maxblk + S - 1) / S;
-  plan->split_blocks = split_blocks;
+  plan->split_tokens = split_blocks * kBlockSize;
+  if (small) {
+    constexpr int kTilesPerBlock = kBlockSize / kTile;
+    const int64_t tiles = static_cast<int64_t>(maxblk) * kTilesPerBlock;
+    const int64_t want = static_cast<int64_t>(sms) * 4;   // about one tile per block
+    int split_tiles = static_cast<int>((seq_units * tiles + want - 1) / want);
+    if (split_tiles < 1) split_tiles = 1;
+    if (split_tiles < kTilesPerBlock) {
+      S = static_cast<int>((tiles + split_tiles - 1) / split_tiles);
+      plan->split_tokens = split_tiles * kTile;
+    }
+  }
   plan->num_splits = S;
   plan->prefix_offset = 0;
   plan->prefix_splits = 0;
@@ -876,7 +898,7 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
   prm.Hkv = a.Hkv;
   prm.maxblk = a.max_blocks_per_seq;
   prm.num_splits = plan.num_splits;
-  prm.split_blocks = plan.split_blocks;
+  prm.split_tokens = plan.split_tokens;
   prm.head_groups = plan.head_groups;
   prm.num_blocks = a.num_blocks;
   prm.scale_log2 = a.scale * 1.4426950408889634f;

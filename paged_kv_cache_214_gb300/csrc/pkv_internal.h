@@ -90,7 +90,7 @@ int check_decode_args(const DecodeArgs& a, int D, int block_size);
 struct DecodePlan {
   int heads_per_cta;  // G: query heads per kv head that one thread block serves
   int head_groups;    // (Hq/Hkv) / G
-  int split_blocks;   // whole KV blocks per split
+  int split_tokens;   // tokens per split: whole blocks, or whole 64-token tiles
   int num_splits;     // S
   size_t prefix_offset;  // byte offset of the shared-prefix partials (if any)
   int prefix_splits;     // key ranges of the shared-prefix pass

@@ -68,6 +68,17 @@ def test_ragged_tile_tails():
     run_and_check(w, num_splits=2, what="tails S=2")
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (16, 4), (32, 4)])
+def test_small_batch_tile_splits(Hq, Hkv):
+    """Batches too small to fill the GPU with one-block splits split into
+    64-token tiles (ranges that start inside a block); every tile and block
+    residue of the context length."""
+    lens = [1, 63, 64, 65, 200, 256, 257, 700]
+    w = W.make_decode(lens, Hq, Hkv, 24, 3050 + Hq)
+    assert pkv.paged_decode_num_splits(w.B, Hq, Hkv, 128, w.block_tables.shape[1]) == 12
+    run_and_check(w, what=f"tile splits Hq={Hq},Hkv={Hkv}")
+
+
 def test_empty_context_gives_zero_and_neg_inf():
     w = W.make_decode([0, 300, 0], 16, 8, 8, 3100, store_new_token=False)
     dev = "cuda"
