@@ -917,10 +917,12 @@ def run_shared_prefix_profile(args):
                       "unique_GB/s": round(ub, 1)}), flush=True)
 
 
-def run_fp8_decode_profile(args, long_ctx: bool):
+def run_fp8_decode_profile(args, long_ctx: bool, fused_store: bool = False):
     """Small-footprint FP8 decode run for ncu: the decode-b64 shapes (2 query
     heads per kv head) or, with `long_ctx`, 8 sequences of 32k-64k tokens with
-    4 query heads per kv head; pools quantized once with kv_cache_store_fp8."""
+    4 query heads per kv head; pools quantized once with kv_cache_store_fp8.
+    `fused_store`: the decode-b64 step's store of the new tokens and the decode
+    in one launch (paged_decode_attention_fp8_store)."""
     from paged_kv_cache_214_gb300 import pkv
     dev = torch.device("cuda", torch.cuda.current_device())
     if long_ctx:
@@ -930,8 +932,8 @@ def run_fp8_decode_profile(args, long_ctx: bool):
         lens = W._uniform_ints(512, 4096, 64, W.seed_for(2))
         Hq, name = 16, "decode-b64-fp8"
     nblk = sum(-(-L // W.BLOCK_SIZE) for L in lens)
-    w = W.make_decode(lens, Hq, 8, nblk, W.seed_for(2), name=name, store_new_token=False,
-                      pool_device=dev)
+    w = W.make_decode(lens, Hq, 8, nblk, W.seed_for(2), name=name,
+                      store_new_token=fused_store, pool_device=dev)
     k8 = torch.empty((nblk, w.block_size, w.Hkv, w.D), dtype=torch.uint8, device=dev)
     v8 = torch.empty_like(k8)
     ks = vs = 6.0 / 448
@@ -946,9 +948,17 @@ def run_fp8_decode_profile(args, long_ctx: bool):
     ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def call():
-        pkv.paged_decode_attention_fp8(q, k8, v8, tables, ctx, w.scale, ks, vs, out=out,
-                                       lse=lse, workspace=ws, stream=stream)
+    if fused_store:
+        kn, vn, slots = w.k_new.to(dev), w.v_new.to(dev), w.slot_mapping.to(dev)
+
+        def call():
+            pkv.paged_decode_attention_fp8_store(q, kn, vn, slots, k8, v8, tables, ctx, w.scale,
+                                                 ks, vs, out=out, lse=lse, workspace=ws,
+                                                 stream=stream)
+    else:
+        def call():
+            pkv.paged_decode_attention_fp8(q, k8, v8, tables, ctx, w.scale, ks, vs, out=out,
+                                           lse=lse, workspace=ws, stream=stream)
     for _ in range(args.warmup):
         call()
     med, _ = _time_calls(call, args.steps, stream)
@@ -956,6 +966,88 @@ def run_fp8_decode_profile(args, long_ctx: bool):
     gbs = decode_bytes(w, kv_elem_bytes=1) / (med / 1e3) / 1e9
     print(json.dumps({"workload": w.name, "us": round(med * 1e3, 2), "GB/s": round(gbs, 1)}),
           flush=True)
+
+
+def run_long_decode_profile(args):
+    """Small-footprint long-context decode run for ncu: the first 2 sequences
+    of long-decode-b8 (32k-131k tokens) in a pool trimmed to their blocks,
+    with the 37 splits the planner picks for the full 8-sequence batch (the
+    split-K path with many splits and the log-sum-exp merge)."""
+    from paged_kv_cache_214_gb300 import pkv
+    dev = torch.device("cuda", torch.cuda.current_device())
+    lens = W._uniform_ints(32768, 131072, 8, W.seed_for(5))[:2]
+    nblk = sum(-(-L // W.BLOCK_SIZE) for L in lens)
+    w = W.make_decode(lens, 32, 8, nblk, W.seed_for(5), name="long-decode-b8-2seq",
+                      store_new_token=False, pool_device=dev, max_blocks_per_seq=512)
+    q, tables, ctx = w.q.to(dev), w.block_tables.to(dev), w.context_lens.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    need = pkv.paged_decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, tables.shape[1],
+                                            num_splits=37)
+    ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        pkv.paged_decode_attention(q, w.k_cache, w.v_cache, tables, ctx, w.scale, out=out,
+                                   lse=lse, workspace=ws, num_splits=37, stream=stream)
+    for _ in range(args.warmup):
+        call()
+    med, _ = _time_calls(call, args.steps, stream)
+    assert pkv.get_device_error() == pkv.PKV_OK
+    gbs = decode_bytes(w) / (med / 1e3) / 1e9
+    print(json.dumps({"workload": w.name, "us": round(med * 1e3, 2), "GB/s": round(gbs, 1)}),
+          flush=True)
+
+
+def run_verify_profile(args):
+    """Small-footprint speculative-verify run for ncu: verify-b64-q4 (the
+    decode-b64 contexts with 4 proposed tokens each) in a pool trimmed to the
+    blocks it uses, through paged_decode_attention_multiquery."""
+    from paged_kv_cache_214_gb300 import pkv
+    dev = torch.device("cuda", torch.cuda.current_device())
+    qn = 4
+    lens = W._uniform_ints(512, 4096, 64, W.seed_for(2))
+    nblk = sum(-(-L // W.BLOCK_SIZE) for L in lens)
+    w = W.make_prefill([L - qn for L in lens], [qn] * len(lens), 16, 8, nblk,
+                       W.seed_for(2) + 1, name="verify-b64-q4", pool_device=dev)
+    q = w.q.to(dev).view(w.B, qn, w.Hq, w.D)
+    tables = w.block_tables.to(dev)
+    ctx = torch.tensor(w.k_lens, dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, qn, w.Hq), dtype=torch.float32, device=dev)
+    need = pkv.paged_decode_multiquery_workspace_bytes(w.B, qn, w.Hq, w.Hkv, w.D,
+                                                       tables.shape[1])
+    ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        pkv.paged_decode_attention_multiquery(q, w.k_cache, w.v_cache, tables, ctx, w.scale,
+                                              out=out, lse=lse, workspace=ws, stream=stream)
+    for _ in range(args.warmup):
+        call()
+    med, _ = _time_calls(call, args.steps, stream)
+    assert pkv.get_device_error() == pkv.PKV_OK
+    print(json.dumps({"workload": w.name, "us": round(med * 1e3, 2)}), flush=True)
+
+
+def run_tiny_profile(args):
+    """tiny-decode for ncu: the 4-sequence decode (64-token splits)."""
+    from paged_kv_cache_214_gb300 import pkv
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = W.config_workload(1, pool_device=dev)
+    q, tables, ctx = w.q.to(dev), w.block_tables.to(dev), w.context_lens.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        pkv.paged_decode_attention(q, w.k_cache, w.v_cache, tables, ctx, w.scale, out=out,
+                                   lse=lse, stream=stream)
+    for _ in range(args.warmup):
+        call()
+    med, _ = _time_calls(call, args.steps, stream)
+    assert pkv.get_device_error() == pkv.PKV_OK
+    print(json.dumps({"workload": w.name, "us": round(med * 1e3, 2)}), flush=True)
 
 
 def main():
@@ -968,7 +1060,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-kernel", default="decode",
                     choices=["decode", "prefill", "shared-prefix", "fp8-decode",
-                             "fp8-decode-long"],
+                             "fp8-decode-store", "fp8-decode-long", "long-decode", "verify",
+                             "tiny"],
                     help="with --profile: which kernel the run exercises")
     ap.add_argument("--profile", action="store_true",
                     help="small-footprint run for ncu: one batch, trimmed pool, "
@@ -986,8 +1079,18 @@ def main():
     if args.profile_kernel == "shared-prefix":
         run_shared_prefix_profile(args)
         return
-    if args.profile_kernel in ("fp8-decode", "fp8-decode-long"):
-        run_fp8_decode_profile(args, args.profile_kernel == "fp8-decode-long")
+    if args.profile_kernel in ("fp8-decode", "fp8-decode-long", "fp8-decode-store"):
+        run_fp8_decode_profile(args, args.profile_kernel == "fp8-decode-long",
+                               fused_store=args.profile_kernel == "fp8-decode-store")
+        return
+    if args.profile_kernel == "long-decode":
+        run_long_decode_profile(args)
+        return
+    if args.profile_kernel == "verify":
+        run_verify_profile(args)
+        return
+    if args.profile_kernel == "tiny":
+        run_tiny_profile(args)
         return
     if args.impl == "reference":
         res = run_reference(args, world, rank)
