@@ -119,13 +119,9 @@ class ClockSampler:
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
-        # nvidia-smi's start-up (library load, device attach) must not overlap
-        # the timed region: wait (at most 5 s) for its first sample
-        t0 = time.perf_counter()
-        while self.proc is not None and time.perf_counter() - t0 < 5.0:
-            if self.proc.poll() is not None or os.path.getsize(self.path) > 0:
-                break
-            time.sleep(0.01)
+        # nvidia-smi's start-up (library load, device attach) runs before the
+        # warm-up, not inside the timed region
+        time.sleep(0.3)
 
     def stop(self):
         if self.proc is None:
