@@ -15,9 +15,13 @@
 //   The range's K and V stream through a ring of shared-memory stages with
 //   TMA (64 tokens x 128 dims per stage, 128-byte swizzle) and mbarrier
 //   completion: bf16 pools 3 stages, each operand two 64-dim boxes; E4M3
-//   pools (one byte per element) 4 stages of one 128-byte box per operand.
-//   Lane 0 of the issuing warps copies one box each and refills the stage
-//   released one tile earlier.
+//   pools (one byte per element) one 128-byte box per operand, 4 stages (or
+//   6 with a producer warp, below).
+//   Copies: a fifth warp (the producer) copies whole stages and refills each
+//   one as soon as every consumer warp has released it (bf16 pools, and E4M3
+//   pools with splits of 8 blocks or more); otherwise (E4M3, shorter splits,
+//   three blocks per SM) lane 0 of the issuing consumer warps copies one box
+//   each and refills the stage released one tile earlier.
 //   Four warps consume, warp w taking tokens [16w, 16w+16) of every stage.
 //   Both contractions run on the warp-level tensor-core MMA (m16n8k16,
 //   16-bit operands, fp32 accumulation) with the G query heads as MMA rows:
@@ -154,23 +158,26 @@ __device__ __forceinline__ void merge_row(const float* lrow, const float* orow, 
 }
 
 // Pipeline geometry per element type.  bf16: 3 stages of 64 tokens, each
-// operand two 64-dim boxes (four copies per stage, one per warp).  FP8 (E4M3,
-// one byte per element): a row of 128 dims is one 128-byte box, so a stage of
-// 64 tokens holds 16 KB; 4 stages (64 KB) let three blocks share an SM, and
-// warps 0 and 1 issue the K and the V copy of each stage.
-template <bool kFp8>
+// operand two 64-dim boxes (four copies per stage).  FP8 (E4M3, one byte per
+// element): a row of 128 dims is one 128-byte box, so a stage of 64 tokens
+// holds 16 KB; without a producer warp, 4 stages (64 KB) let three blocks
+// share an SM and warps 0 and 1 issue the K and the V copy of each stage;
+// with one (kProd), 6 stages at two blocks per SM (the fifth warp's registers
+// leave no room for a third block).
+template <bool kFp8, bool kProd = false>
 struct Geo {
-  static constexpr int kStagesN = kFp8 ? 4 : 3;
+  static constexpr int kStagesN = kFp8 ? (kProd ? 6 : 4) : 3;
   static constexpr int kOpBytes = kTile * (kFp8 ? 128 : 256);  // one of K or V for a stage
   static constexpr int kStageB = 2 * kOpBytes;
   static constexpr int kIssuers = kFp8 ? 2 : 4;
 };
-static_assert(Geo<false>::kStagesN == kStages && Geo<false>::kStageB == kStageBytes, "geometry");
+static_assert(Geo<false, true>::kStagesN == kStages && Geo<false, true>::kStageB == kStageBytes,
+              "geometry");
 
-template <int G, bool kFp8 = false>
+template <int G, bool kFp8 = false, bool kProd = false>
 struct SmemLayout {
-  static constexpr int kStages = Geo<kFp8>::kStagesN;
-  static constexpr int kStageBytes = Geo<kFp8>::kStageB;
+  static constexpr int kStages = Geo<kFp8, kProd>::kStagesN;
+  static constexpr int kStageBytes = Geo<kFp8, kProd>::kStageB;
   // [4][G][128] f32, over the stage ring: written only once every warp is
   // done with the stages and no copy is in flight
   static constexpr int kMergeO = 0;
@@ -190,18 +197,255 @@ __device__ __forceinline__ float rescale(float m, float mn) {
   return m == -INFINITY ? 0.f : ex2(m - mn);
 }
 
-// kMQ: several query positions per sequence (q_len > 1); plain decode
-// compiles without the per-row key limits.  kFp8: E4M3 pools.  One kv head
-// per block; G of its query heads.
+// A operand of the score MMA for the lane's row gq from its 16 words of q
+// (bf16 pairs of dims [32c, 32c+32)), and the multiplier that turns a raw
+// score into the log2 domain.  bf16 pools: the words as they are.  E4M3
+// pools: q goes to f16 scaled by the power of two that brings its row maximum
+// into [2^14, 2^15), where every bf16 element down to 2^-32 of that maximum
+// converts exactly; the multiplier undoes that power and applies k_scale.
+// Every lane of the warp takes part (row maxima by shuffles).
+template <bool kFp8>
+__device__ __forceinline__ void q_fragments(const uint32_t (&qw)[16], float scale_log2,
+                                            float k_scale, uint32_t (&qa)[8][2], float& qmul) {
+  if constexpr (kFp8) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      amax = fmaxf(amax, fmaxf(fabsf(bf16lo(qw[i])), fabsf(bf16hi(qw[i]))));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    // amax = f * 2^e, f in [0.5, 1) (e = -126 for zero and subnormals)
+    const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 126;
+    const int sh = min(15 - e, 100);
+    const float up = __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);
+    qmul = scale_log2 * k_scale * __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      qa[m][0] = pack_f16x2(bf16lo(qw[2 * m]) * up, bf16hi(qw[2 * m]) * up);
+      qa[m][1] = pack_f16x2(bf16lo(qw[2 * m + 1]) * up, bf16hi(qw[2 * m + 1]) * up);
+    }
+  } else {
+    qmul = scale_log2;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      qa[m][0] = qw[2 * m];
+      qa[m][1] = qw[2 * m + 1];
+    }
+  }
+}
+
+// One 64-token stage consumed by one warp (see the consumer notes in the
+// kernels below): the scores of the warp's 16 tokens [16 warp, 16 warp + 16)
+// against the G query rows, the online-softmax update of (m_run, l_run, o) and
+// o += P V.  kb / vb: shared addresses of the stage's K and V.  n_valid: tokens
+// of the stage inside the key range.  lim (several query positions only): keys
+// that row gq may see, counted from the stage's first token.
 template <int G, bool kMQ, bool kFp8>
-__global__ void __launch_bounds__(kThreads, 2)
+__device__ __forceinline__ void consume_stage(uint32_t kb, uint32_t vb, int warp, int gq, int c,
+                                              const uint32_t (&qa)[8][2], float qmul,
+                                              int n_valid, int lim, float (&o)[16][4],
+                                              float& m_run, float& l_run) {
+  const int t0 = 16 * warp;
+
+  // scores of token groups n = 0, 1: row (token) t0 + 8n + gq; a
+  // 128-byte row's 16-byte chunk j sits at chunk j ^ (row & 7) = j ^ gq
+  float sc[2][4];
+#pragma unroll
+  for (int n = 0; n < 2; ++n) {
+    uint32_t kw[16];
+    if constexpr (kFp8) {
+      const uint32_t row = kb + (t0 + 8 * n + gq) * 128;
+      const uint4 k0 = lds128(row + (((2 * c) ^ gq) << 4));
+      const uint4 k1 = lds128(row + (((2 * c + 1) ^ gq) << 4));
+      const uint32_t w[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        kw[2 * i] = e4m3x2_lo_to_f16x2(w[i]);
+        kw[2 * i + 1] = e4m3x2_hi_to_f16x2(w[i]);
+      }
+    } else {
+      // dims [32c, 32c+32): half c >> 1, chunks 4 (c & 1) .. + 3
+      const uint32_t row = kb + (c >> 1) * kHalfBytes + (t0 + 8 * n + gq) * 128;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 u = lds128(row + (((4 * (c & 1) + i) ^ gq) << 4));
+        kw[4 * i] = u.x;
+        kw[4 * i + 1] = u.y;
+        kw[4 * i + 2] = u.z;
+        kw[4 * i + 3] = u.w;
+      }
+    }
+    sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+#pragma unroll
+    for (int mm = 0; mm < 8; ++mm)
+      mma_16x8x16<kFp8>(sc[n], qa[mm][0], 0u, qa[mm][1], 0u, kw[2 * mm], kw[2 * mm + 1]);
+  }
+  // online softmax of row gq over the warp's 16 tokens; this lane has
+  // tokens t0 + 8 (i >> 1) + 2c + (i & 1), i = 0..3
+  bool ok[4];
+  float sv[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + 8 * (i >> 1) + 2 * c + (i & 1);
+    ok[i] = t < n_valid && (!kMQ || t < lim);
+    sv[i] = ok[i] ? sc[i >> 1][i & 1] * qmul : -INFINITY;
+  }
+  float mt = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+  mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+  mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+  // the running max moves only when the tile's exceeds it by 2^8; below
+  // that the weights stay within 256 and o is not rescaled
+  if (mt > m_run + 8.f) {
+    const float alpha = rescale(m_run, mt);
+    l_run *= alpha;
+#pragma unroll
+    for (int jn = 0; jn < 16; ++jn) {
+      o[jn][0] *= alpha;
+      o[jn][1] *= alpha;
+      o[jn][2] *= alpha;
+      o[jn][3] *= alpha;
+    }
+    m_run = mt;
+  }
+  float pw[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    pw[i] = ok[i] ? ex2(sv[i] - m_run) : 0.f;
+    l_run += pw[i];
+  }
+  // A operand of P V: k positions 2c, 2c+1 are tokens t0 + 2c, +1 (a0 / a1)
+  // and 2c+8, 2c+9 tokens t0 + 8 + 2c, +1 (a2 / a3)
+  uint32_t ph0, pl0, ph2, pl2;
+  split_pair<kFp8>(pw[0], pw[1], ph0, pl0);
+  split_pair<kFp8>(pw[2], pw[3], ph2, pl2);
+
+  // values: this lane gives B column gq at k positions 2c, 2c+1 (tokens
+  // A, B) and 2c+8, 2c+9 (tokens C, D).  Tokens past the context are
+  // zeroed: stale slots may hold NaN patterns.
+  if constexpr (kFp8) {
+    // column gq of n-tile jn is dim 16 gq + jn: byte jn of the chunk
+    uint32_t vw[4][4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int t = t0 + 8 * (k >> 1) + 2 * c + (k & 1);
+      uint4 v = lds128(vb + t * 128 + ((gq ^ (t & 7)) << 4));
+      if (t >= n_valid) v = make_uint4(0u, 0u, 0u, 0u);
+      vw[k][0] = v.x;
+      vw[k][1] = v.y;
+      vw[k][2] = v.z;
+      vw[k][3] = v.w;
+    }
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      // bytes 4wi..4wi+3 of two tokens interleaved: n-tiles 4wi..4wi+3
+      const uint32_t ab01 = __byte_perm(vw[0][wi], vw[1][wi], 0x5140);
+      const uint32_t ab23 = __byte_perm(vw[0][wi], vw[1][wi], 0x7362);
+      const uint32_t cd01 = __byte_perm(vw[2][wi], vw[3][wi], 0x5140);
+      const uint32_t cd23 = __byte_perm(vw[2][wi], vw[3][wi], 0x7362);
+      mma_16x8x16<true>(o[4 * wi], ph0, pl0, ph2, pl2, e4m3x2_lo_to_f16x2(ab01),
+                        e4m3x2_lo_to_f16x2(cd01));
+      mma_16x8x16<true>(o[4 * wi + 1], ph0, pl0, ph2, pl2, e4m3x2_hi_to_f16x2(ab01),
+                        e4m3x2_hi_to_f16x2(cd01));
+      mma_16x8x16<true>(o[4 * wi + 2], ph0, pl0, ph2, pl2, e4m3x2_lo_to_f16x2(ab23),
+                        e4m3x2_lo_to_f16x2(cd23));
+      mma_16x8x16<true>(o[4 * wi + 3], ph0, pl0, ph2, pl2, e4m3x2_hi_to_f16x2(ab23),
+                        e4m3x2_hi_to_f16x2(cd23));
+    }
+  } else {
+    // dims [16 gq, 16 gq + 16): half gq >> 2, chunks 2 (gq & 3) + {0, 1},
+    // the two loaded in the order (gq & 1, 1 - (gq & 1)) so that each load
+    // instruction touches all eight chunk positions; load i then holds
+    // dims 16 gq + 8 (i ^ (gq & 1)) + 0..7, and column gq of n-tile jn is
+    // dim 16 gq + (jn ^ 8 (gq & 1))
+    uint32_t vw[4][8];
+    const uint32_t vhalf = vb + (gq >> 2) * kHalfBytes;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int t = t0 + 8 * (k >> 1) + 2 * c + (k & 1);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int chunk = 2 * (gq & 3) + (i ^ (gq & 1));
+        uint4 v = lds128(vhalf + t * 128 + ((chunk ^ (t & 7)) << 4));
+        if (t >= n_valid) v = make_uint4(0u, 0u, 0u, 0u);
+        vw[k][4 * i] = v.x;
+        vw[k][4 * i + 1] = v.y;
+        vw[k][4 * i + 2] = v.z;
+        vw[k][4 * i + 3] = v.w;
+      }
+    }
+#pragma unroll
+    for (int jn = 0; jn < 16; ++jn) {
+      // word jn >> 1 holds the dims 2 (jn >> 1), +1 of load jn >> 3
+      const uint32_t sel = (jn & 1) ? 0x7632u : 0x5410u;
+      const uint32_t b0 = __byte_perm(vw[0][jn >> 1], vw[1][jn >> 1], sel);
+      const uint32_t b1 = __byte_perm(vw[2][jn >> 1], vw[3][jn >> 1], sel);
+      mma_16x8x16<false>(o[jn], ph0, pl0, ph2, pl2, b0, b1);
+    }
+  }
+}
+
+// Fused store, by one whole warp: the new token's row of kv head kvh0 goes to
+// slot sl, which must be the slot of position pos = ctx - 1 (block blk of the
+// sequence's table): no other range reads it, and blocks of other head
+// groups write the same bytes.  Any other slot is reported and not written.
+// bf16: lanes 0-15 copy the K row, 16-31 the V row, 16 bytes each.  E4M3:
+// lanes 0-7 quantize 16 elements of the K row, 8-15 of the V row, exactly as
+// kv_cache_store_fp8 does (fp32 product with the binary32 reciprocal scale,
+// nearest code, ties to even, saturating).  Each writing lane then orders its
+// write before later tensor copies (async proxy) of the same bytes.
+template <bool kFp8>
+__device__ __forceinline__ void store_new_row(const DecodeParams& p, int b, int kvh0, int sl,
+                                              int blk, int pos, int lane) {
+  if (sl != blk * kBlockSize + pos % kBlockSize) {
+    if (lane == 0) record_error(p.err, kErrIndex);
+    return;
+  }
+  const int64_t row_idx = static_cast<int64_t>(sl) * p.Hkv + kvh0;
+  if constexpr (kFp8) {
+    if (lane < 16) {
+      const bool is_k = lane < 8;
+      const __nv_bfloat16* row = is_k ? p.k_new + b * p.k_new_stride
+                                      : p.v_new + b * p.v_new_stride;
+      const uint4* src = reinterpret_cast<const uint4*>(row + kvh0 * kHeadDim) + 2 * (lane & 7);
+      const uint4 x0 = __ldg(src), x1 = __ldg(src + 1);
+      const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const float inv = is_k ? p.k_inv : p.v_inv;
+      uint32_t cw[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t c0 = e4m3x2_from_f32(bf16lo(w[2 * j]) * inv, bf16hi(w[2 * j]) * inv);
+        const uint32_t c1 =
+            e4m3x2_from_f32(bf16lo(w[2 * j + 1]) * inv, bf16hi(w[2 * j + 1]) * inv);
+        cw[j] = c0 | (c1 << 16);
+      }
+      uint4* pool = is_k ? p.k_pool : p.v_pool;
+      pool[row_idx * (kHeadDim / 16) + (lane & 7)] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      fence_proxy_async_global();
+    }
+  } else {
+    const __nv_bfloat16* row = lane < 16 ? p.k_new + b * p.k_new_stride
+                                         : p.v_new + b * p.v_new_stride;
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + kvh0 * kHeadDim) + (lane & 15));
+    uint4* pool = lane < 16 ? p.k_pool : p.v_pool;
+    pool[row_idx * (kHeadDim / 8) + (lane & 15)] = v;
+    fence_proxy_async_global();
+  }
+}
+
+// kMQ: several query positions per sequence (q_len > 1); plain decode
+// compiles without the per-row key limits.  kFp8: E4M3 pools.  kProd: a fifth
+// warp issues every copy, so that no consumer warp waits for the others to
+// release a stage before its next tile.  One kv head per block; G of its
+// query heads.
+template <int G, bool kMQ, bool kFp8, bool kProd>
+__global__ void __launch_bounds__(kProd ? kThreads + 32 : kThreads, 2)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
-  using L = SmemLayout<G, kFp8>;
-  constexpr int kStagesN = Geo<kFp8>::kStagesN;
-  constexpr int kStageB = Geo<kFp8>::kStageB;
-  constexpr int kOpBytes = Geo<kFp8>::kOpBytes;
-  constexpr int kIssuers = Geo<kFp8>::kIssuers;
+  using L = SmemLayout<G, kFp8, kProd>;
+  constexpr int kStagesN = Geo<kFp8, kProd>::kStagesN;
+  constexpr int kStageB = Geo<kFp8, kProd>::kStageB;
+  constexpr int kOpBytes = Geo<kFp8, kProd>::kOpBytes;
+  constexpr int kIssuers = Geo<kFp8, kProd>::kIssuers;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -278,7 +522,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 
   if (ctx == P) {  // nothing past the prefix: out = the prefix's result (or 0, -inf)
     if (P > 0) {
-      for (int r = warp; r < G; r += kConsumerWarps) {
+      for (int r = warp; r < G && warp < kConsumerWarps; r += kConsumerWarps) {
         const int64_t row = static_cast<int64_t>(b) * p.Hq + qhead(r);
         const int np = p.prefix_splits;
         const int64_t prow = phys_row(qhead(r));
@@ -287,7 +531,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       }
       return;
     }
-    for (int i = tid; i < G * kHeadDim; i += kThreads) {
+    for (int i = tid; i < G * kHeadDim; i += blockDim.x) {
       const int r = i / kHeadDim, d = i % kHeadDim;
       p.out[phys_row(qhead(r)) * kHeadDim + d] = __float2bfloat16_rn(0.f);
     }
@@ -299,12 +543,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   const int tok_end = min(ctx, tok_begin + split_tokens);
   const int n_tiles = (tok_end - tok_begin + kTile - 1) / kTile;
 
-  // bf16: every warp is a producer for one quarter of each stage (warp w
-  // loads K dims [0,64), K [64,128), V [0,64), V [64,128) for w = 0..3): one
-  // thread streams its tensor copies one after another at a few hundred cycles
-  // each, so four issuing threads land a stage sooner than one.  E4M3: warps 0
-  // and 1 copy the stage's K and V box.  Lane 0 of each issuing warp fills its
-  // part of the ring up front and refills the stage released one tile earlier.
+  // kProd: lane 0 of the producer warp copies whole stages (bf16: K dims
+  // [0,64), [64,128), V [0,64), [64,128); E4M3: the K and the V box), filling
+  // the ring up front and refilling each stage as soon as every consumer warp
+  // has released it.  Otherwise the consumer warps copy: bf16: warp w loads
+  // the w-th of those four boxes; E4M3: warps 0 and 1 the K and the V box.
+  // Lane 0 of each issuing warp fills its part of the ring up front and
+  // refills the stage released one tile earlier.
   const uint64_t policy = l2_policy_evict_first();
   const int withhold = withheld_tile();   // test hook: tiles from here on are never copied
   auto issue = [&](int it) {
@@ -318,7 +563,16 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       flags[0] = 1;
       return;
     }
-    if constexpr (kFp8) {
+    if constexpr (kProd) {
+      const uint32_t dst = smem_addr(smem + s * kStageB);
+      mbar_arrive_expect_tx(full_bar(s), kStageB);
+      tma_load_3d_hint(dst, &kmap, full_bar(s), 0, kvh0, slot, policy);
+      if constexpr (!kFp8)
+        tma_load_3d_hint(dst + kHalfBytes, &kmap, full_bar(s), 64, kvh0, slot, policy);
+      tma_load_3d_hint(dst + kOpBytes, &vmap, full_bar(s), 0, kvh0, slot, policy);
+      if constexpr (!kFp8)
+        tma_load_3d_hint(dst + kOpBytes + kHalfBytes, &vmap, full_bar(s), 64, kvh0, slot, policy);
+    } else if constexpr (kFp8) {
       // warp 0: the K tile, warp 1: the V tile (one 128-byte-wide box each)
       const uint32_t dst = smem_addr(smem + s * kStageB) + warp * kOpBytes;
       mbar_arrive_expect_tx(full_bar(s), kOpBytes);
@@ -339,7 +593,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   if (warp == 0) {
     if (lane == 0) {
       for (int s = 0; s < kStagesN; ++s) {
-        mbar_init(full_bar(s), kIssuers);         // one arrival per issuing warp
+        mbar_init(full_bar(s), kProd ? 1 : kIssuers);  // one arrival per issuing warp
         mbar_init(empty_bar(s), kConsumerWarps);
       }
       mbar_init(stored_bar, 1);
@@ -361,60 +615,19 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   }
   __syncthreads();
   if (store_here && warp == 1) {
-    // Warp 1 writes the new token's row of this kv head at its slot, which
-    // must be the slot of position ctx - 1: no other range reads it, and
-    // blocks of other head groups write the same bytes.  Any other slot is
-    // reported and not written.  bf16: lanes 0-15 copy the K row, 16-31 the V
-    // row, 16 bytes each.  E4M3: lanes 0-7 quantize 16 elements of the K row,
-    // 8-15 of the V row, exactly as kv_cache_store_fp8 does (fp32 product with
-    // the binary32 reciprocal scale, nearest code, ties to even, saturating).
-    // Then the warp tells the issuing lanes, one of which waits for it before
-    // copying the tile that holds the row.
+    // Warp 1 writes the new token's row of this kv head at its slot (see
+    // store_new_row), then tells the issuing lanes, one of which waits for it
+    // before copying the tile that holds the row.
     const int sl = __ldg(p.new_slots + b);
     if (sl >= 0) {
       const int pos = ctx - 1;
-      const int blk = sblk[pos / kBlockSize - blk_begin];
-      if (sl == blk * kBlockSize + pos % kBlockSize) {
-        const int64_t row_idx = static_cast<int64_t>(sl) * p.Hkv + kvh0;
-        if constexpr (kFp8) {
-          if (lane < 16) {
-            const bool is_k = lane < 8;
-            const __nv_bfloat16* row = is_k ? p.k_new + b * p.k_new_stride
-                                            : p.v_new + b * p.v_new_stride;
-            const uint4* src = reinterpret_cast<const uint4*>(row + kvh0 * kHeadDim) +
-                               2 * (lane & 7);
-            const uint4 x0 = __ldg(src), x1 = __ldg(src + 1);
-            const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            const float inv = is_k ? p.k_inv : p.v_inv;
-            uint32_t c[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint32_t c0 = e4m3x2_from_f32(bf16lo(w[2 * j]) * inv, bf16hi(w[2 * j]) * inv);
-              const uint32_t c1 =
-                  e4m3x2_from_f32(bf16lo(w[2 * j + 1]) * inv, bf16hi(w[2 * j + 1]) * inv);
-              c[j] = c0 | (c1 << 16);
-            }
-            uint4* pool = is_k ? p.k_pool : p.v_pool;
-            pool[row_idx * (kHeadDim / 16) + (lane & 7)] = make_uint4(c[0], c[1], c[2], c[3]);
-            fence_proxy_async_global();
-          }
-        } else {
-          const __nv_bfloat16* row = lane < 16 ? p.k_new + b * p.k_new_stride
-                                               : p.v_new + b * p.v_new_stride;
-          const uint4 v =
-              __ldg(reinterpret_cast<const uint4*>(row + kvh0 * kHeadDim) + (lane & 15));
-          uint4* pool = lane < 16 ? p.k_pool : p.v_pool;
-          pool[row_idx * (kHeadDim / 8) + (lane & 15)] = v;
-          fence_proxy_async_global();
-        }
-      } else if (lane == 0) {
-        record_error(p.err, kErrIndex);
-      }
+      store_new_row<kFp8>(p, b, kvh0, sl, sblk[pos / kBlockSize - blk_begin], pos, lane);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(stored_bar);
   }
-  if (lane == 0 && warp < kIssuers)
+  const bool prodw = kProd && warp == kConsumerWarps;  // the producer warp
+  if (lane == 0 && (kProd ? prodw : warp < kIssuers))
     for (int it = 0; it < kStagesN && it < n_tiles; ++it) issue(it);
 
   {
@@ -437,6 +650,28 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     // (f16) significant bits.
     const int gq = lane >> 2;
     const int c = lane & 3;
+    // o[jn][0..1]: rows gq, o[jn][2..3]: rows gq + 8 (the weight remainders);
+    // summed when the loop ends.  Output column n of n-tile jn is dim
+    // vdim(n, jn) below.
+    float o[16][4];
+#pragma unroll
+    for (int jn = 0; jn < 16; ++jn) o[jn][0] = o[jn][1] = o[jn][2] = o[jn][3] = 0.f;
+    float m_run = -INFINITY;  // log2-domain running max of row gq
+    float l_run = 0.f;        // sum of the weights of this lane's tokens
+    if (prodw) {
+      if (lane == 0) {
+        for (int it = kStagesN; it < n_tiles && !flags[0]; ++it) {
+          const int pv = it - kStagesN;
+          if (!mbar_wait(empty_bar(pv % kStagesN), (pv / kStagesN) & 1)) {
+            record_error(p.err, kErrTimeout);
+            flags[0] = 1;
+            break;
+          }
+          issue(it);
+        }
+      }
+      __syncwarp();
+    } else {
     uint32_t qa[8][2];
     float qmul;
     {
@@ -456,43 +691,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
         for (int i = 0; i < 16; ++i) qw[i] = 0u;
       }
-      if constexpr (kFp8) {
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          amax = fmaxf(amax, fmaxf(fabsf(bf16lo(qw[i])), fabsf(bf16hi(qw[i]))));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        // amax = f * 2^e, f in [0.5, 1) (e = -126 for zero and subnormals)
-        const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 126;
-        const int sh = min(15 - e, 100);
-        const float up = __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);
-        qmul = p.scale_log2 * p.k_scale *
-               __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          qa[m][0] = pack_f16x2(bf16lo(qw[2 * m]) * up, bf16hi(qw[2 * m]) * up);
-          qa[m][1] = pack_f16x2(bf16lo(qw[2 * m + 1]) * up, bf16hi(qw[2 * m + 1]) * up);
-        }
-      } else {
-        qmul = p.scale_log2;
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          qa[m][0] = qw[2 * m];
-          qa[m][1] = qw[2 * m + 1];
-        }
-      }
+      q_fragments<kFp8>(qw, p.scale_log2, p.k_scale, qa, qmul);
     }
     // keys of this split row gq may see (several query positions only)
     const int lim = kMQ ? key_limit(qhead(gq < G ? gq : 0)) - tok_begin : 0;
-    // o[jn][0..1]: rows gq, o[jn][2..3]: rows gq + 8 (the weight remainders);
-    // summed when the loop ends.  Output column n of n-tile jn is dim
-    // vdim(n, jn) below.
-    float o[16][4];
-#pragma unroll
-    for (int jn = 0; jn < 16; ++jn) o[jn][0] = o[jn][1] = o[jn][2] = o[jn][3] = 0.f;
-    float m_run = -INFINITY;  // log2-domain running max of row gq
-    float l_run = 0.f;        // sum of the weights of this lane's tokens
 
     for (int it = 0; it < n_tiles; ++it) {
       const int s = it % kStagesN;
@@ -504,151 +706,15 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       }
       const int n_valid = min(kTile, tok_end - (tok_begin + it * kTile));
       const uint32_t kb = smem_addr(smem + s * kStageB);
-      const uint32_t vb = kb + kOpBytes;
-      const int t0 = 16 * warp;
-
-      // scores of token groups n = 0, 1: row (token) t0 + 8n + gq; a
-      // 128-byte row's 16-byte chunk j sits at chunk j ^ (row & 7) = j ^ gq
-      float sc[2][4];
-#pragma unroll
-      for (int n = 0; n < 2; ++n) {
-        uint32_t kw[16];
-        if constexpr (kFp8) {
-          const uint32_t row = kb + (t0 + 8 * n + gq) * 128;
-          const uint4 k0 = lds128(row + (((2 * c) ^ gq) << 4));
-          const uint4 k1 = lds128(row + (((2 * c + 1) ^ gq) << 4));
-          const uint32_t w[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            kw[2 * i] = e4m3x2_lo_to_f16x2(w[i]);
-            kw[2 * i + 1] = e4m3x2_hi_to_f16x2(w[i]);
-          }
-        } else {
-          // dims [32c, 32c+32): half c >> 1, chunks 4 (c & 1) .. + 3
-          const uint32_t row = kb + (c >> 1) * kHalfBytes + (t0 + 8 * n + gq) * 128;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint4 u = lds128(row + (((4 * (c & 1) + i) ^ gq) << 4));
-            kw[4 * i] = u.x;
-            kw[4 * i + 1] = u.y;
-            kw[4 * i + 2] = u.z;
-            kw[4 * i + 3] = u.w;
-          }
-        }
-        sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-#pragma unroll
-        for (int mm = 0; mm < 8; ++mm)
-          mma_16x8x16<kFp8>(sc[n], qa[mm][0], 0u, qa[mm][1], 0u, kw[2 * mm], kw[2 * mm + 1]);
-      }
-      // online softmax of row gq over the warp's 16 tokens; this lane has
-      // tokens t0 + 8 (i >> 1) + 2c + (i & 1), i = 0..3
-      bool ok[4];
-      float sv[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int t = t0 + 8 * (i >> 1) + 2 * c + (i & 1);
-        ok[i] = t < n_valid && (!kMQ || it * kTile + t < lim);
-        sv[i] = ok[i] ? sc[i >> 1][i & 1] * qmul : -INFINITY;
-      }
-      float mt = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-      // the running max moves only when the tile's exceeds it by 2^8; below
-      // that the weights stay within 256 and o is not rescaled
-      if (mt > m_run + 8.f) {
-        const float alpha = rescale(m_run, mt);
-        l_run *= alpha;
-#pragma unroll
-        for (int jn = 0; jn < 16; ++jn) {
-          o[jn][0] *= alpha;
-          o[jn][1] *= alpha;
-          o[jn][2] *= alpha;
-          o[jn][3] *= alpha;
-        }
-        m_run = mt;
-      }
-      float pw[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        pw[i] = ok[i] ? ex2(sv[i] - m_run) : 0.f;
-        l_run += pw[i];
-      }
-      // A operand of P V: k positions 2c, 2c+1 are tokens t0 + 2c, +1 (a0 / a1)
-      // and 2c+8, 2c+9 tokens t0 + 8 + 2c, +1 (a2 / a3)
-      uint32_t ph0, pl0, ph2, pl2;
-      split_pair<kFp8>(pw[0], pw[1], ph0, pl0);
-      split_pair<kFp8>(pw[2], pw[3], ph2, pl2);
-
-      // values: this lane gives B column gq at k positions 2c, 2c+1 (tokens
-      // A, B) and 2c+8, 2c+9 (tokens C, D).  Tokens past the context are
-      // zeroed: stale slots may hold NaN patterns.
-      if constexpr (kFp8) {
-        // column gq of n-tile jn is dim 16 gq + jn: byte jn of the chunk
-        uint32_t vw[4][4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int t = t0 + 8 * (k >> 1) + 2 * c + (k & 1);
-          uint4 v = lds128(vb + t * 128 + ((gq ^ (t & 7)) << 4));
-          if (t >= n_valid) v = make_uint4(0u, 0u, 0u, 0u);
-          vw[k][0] = v.x;
-          vw[k][1] = v.y;
-          vw[k][2] = v.z;
-          vw[k][3] = v.w;
-        }
-#pragma unroll
-        for (int wi = 0; wi < 4; ++wi) {
-          // bytes 4wi..4wi+3 of two tokens interleaved: n-tiles 4wi..4wi+3
-          const uint32_t ab01 = __byte_perm(vw[0][wi], vw[1][wi], 0x5140);
-          const uint32_t ab23 = __byte_perm(vw[0][wi], vw[1][wi], 0x7362);
-          const uint32_t cd01 = __byte_perm(vw[2][wi], vw[3][wi], 0x5140);
-          const uint32_t cd23 = __byte_perm(vw[2][wi], vw[3][wi], 0x7362);
-          mma_16x8x16<true>(o[4 * wi], ph0, pl0, ph2, pl2, e4m3x2_lo_to_f16x2(ab01),
-                            e4m3x2_lo_to_f16x2(cd01));
-          mma_16x8x16<true>(o[4 * wi + 1], ph0, pl0, ph2, pl2, e4m3x2_hi_to_f16x2(ab01),
-                            e4m3x2_hi_to_f16x2(cd01));
-          mma_16x8x16<true>(o[4 * wi + 2], ph0, pl0, ph2, pl2, e4m3x2_lo_to_f16x2(ab23),
-                            e4m3x2_lo_to_f16x2(cd23));
-          mma_16x8x16<true>(o[4 * wi + 3], ph0, pl0, ph2, pl2, e4m3x2_hi_to_f16x2(ab23),
-                            e4m3x2_hi_to_f16x2(cd23));
-        }
-      } else {
-        // dims [16 gq, 16 gq + 16): half gq >> 2, chunks 2 (gq & 3) + {0, 1},
-        // the two loaded in the order (gq & 1, 1 - (gq & 1)) so that each load
-        // instruction touches all eight chunk positions; load i then holds
-        // dims 16 gq + 8 (i ^ (gq & 1)) + 0..7, and column gq of n-tile jn is
-        // dim 16 gq + (jn ^ 8 (gq & 1))
-        uint32_t vw[4][8];
-        const uint32_t vhalf = vb + (gq >> 2) * kHalfBytes;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int t = t0 + 8 * (k >> 1) + 2 * c + (k & 1);
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const int chunk = 2 * (gq & 3) + (i ^ (gq & 1));
-            uint4 v = lds128(vhalf + t * 128 + ((chunk ^ (t & 7)) << 4));
-            if (t >= n_valid) v = make_uint4(0u, 0u, 0u, 0u);
-            vw[k][4 * i] = v.x;
-            vw[k][4 * i + 1] = v.y;
-            vw[k][4 * i + 2] = v.z;
-            vw[k][4 * i + 3] = v.w;
-          }
-        }
-#pragma unroll
-        for (int jn = 0; jn < 16; ++jn) {
-          // word jn >> 1 holds the dims 2 (jn >> 1), +1 of load jn >> 3
-          const uint32_t sel = (jn & 1) ? 0x7632u : 0x5410u;
-          const uint32_t b0 = __byte_perm(vw[0][jn >> 1], vw[1][jn >> 1], sel);
-          const uint32_t b1 = __byte_perm(vw[2][jn >> 1], vw[3][jn >> 1], sel);
-          mma_16x8x16<false>(o[jn], ph0, pl0, ph2, pl2, b0, b1);
-        }
-      }
+      consume_stage<G, kMQ, kFp8>(kb, kb + kOpBytes, warp, gq, c, qa, qmul, n_valid,
+                                  lim - it * kTile, o, m_run, l_run);
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(empty_bar(s));
         // refill the stage released one tile ago: by now every warp has
         // usually released it too, so the issuing lanes seldom wait
         const int pv = it - 1;
-        if (warp < kIssuers && pv >= 0 && pv + kStagesN < n_tiles && !flags[0]) {
+        if (!kProd && warp < kIssuers && pv >= 0 && pv + kStagesN < n_tiles && !flags[0]) {
           if (mbar_wait(empty_bar(pv % kStagesN), (pv / kStagesN) & 1)) {
             issue(pv + kStagesN);
           } else {
@@ -658,6 +724,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
         }
       }
       __syncwarp();
+    }
     }
 
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
@@ -674,7 +741,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       }
     }
     __syncthreads();
-    if (gq < G) {
+    if (gq < G && !prodw) {
       // this lane's output columns: n = 2c at dims 32c + jn and n = 2c + 1 at
       // dims 32c + 16 + jn (bf16: 32c + 16 + (jn ^ 8))
       float* dst = merge_o + (warp * G + gq) * kHeadDim + 32 * c;
@@ -691,6 +758,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   }
 
   __syncthreads();
+  if (prodw) return;
 
   // ---------------------------------------------------------------- epilogue
   // thread tid (0..127) owns dim d = tid of every head
@@ -751,23 +819,24 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   if (tid == 0) *counter = 0u;  // ready for the next call
 }
 
-template <int G, bool kMQ, bool kFp8 = false>
+template <int G, bool kMQ, bool kFp8, bool kProd>
 int launch_g(const DecodeArgs& a, const DecodePlan& plan, const DecodeParams& prm,
              const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t stream) {
-  using L = SmemLayout<G, kFp8>;
+  using L = SmemLayout<G, kFp8, kProd>;
   static_assert(L::kBytes <= 113 * 1024, "two blocks per SM must fit");
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(paged_decode_kernel<G, kMQ, kFp8>,
+    if (cudaFuncSetAttribute(paged_decode_kernel<G, kMQ, kFp8, kProd>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::kBytes) != cudaSuccess)
       return PKV_ERR_LAUNCH;
     attr_set[dev] = true;
   }
   dim3 grid(plan.num_splits, a.Hkv * plan.head_groups, a.B);
-  paged_decode_kernel<G, kMQ, kFp8><<<grid, kThreads, L::kBytes, stream>>>(km, vm, prm);
+  paged_decode_kernel<G, kMQ, kFp8, kProd>
+      <<<grid, kProd ? kThreads + 32 : kThreads, L::kBytes, stream>>>(km, vm, prm);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }
 
@@ -936,27 +1005,41 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
     prm.ws_lse = nullptr;
     prm.ws_count = nullptr;
   }
+  // bf16 pools: the producer-warp form (two blocks per SM either way).  E4M3
+  // pools: three blocks per SM of the consumer-issued form, or two of the
+  // producer-warp form with a deeper ring; the latter wins once a split is
+  // long enough (measured on GB300: 8-block splits of the 32K-128K-token
+  // contexts 6% faster, 4-block splits of 512-4096-token contexts 1.5% slower).
   if (a.fp8) {
+    const bool prod = plan.split_tokens >= 8 * kBlockSize;
     switch (plan.heads_per_cta) {
-      case 8: return launch_g<8, false, true>(a, plan, prm, km, vm, stream);
-      case 4: return launch_g<4, false, true>(a, plan, prm, km, vm, stream);
-      case 2: return launch_g<2, false, true>(a, plan, prm, km, vm, stream);
-      default: return launch_g<1, false, true>(a, plan, prm, km, vm, stream);
+      case 8:
+        return prod ? launch_g<8, false, true, true>(a, plan, prm, km, vm, stream)
+                    : launch_g<8, false, true, false>(a, plan, prm, km, vm, stream);
+      case 4:
+        return prod ? launch_g<4, false, true, true>(a, plan, prm, km, vm, stream)
+                    : launch_g<4, false, true, false>(a, plan, prm, km, vm, stream);
+      case 2:
+        return prod ? launch_g<2, false, true, true>(a, plan, prm, km, vm, stream)
+                    : launch_g<2, false, true, false>(a, plan, prm, km, vm, stream);
+      default:
+        return prod ? launch_g<1, false, true, true>(a, plan, prm, km, vm, stream)
+                    : launch_g<1, false, true, false>(a, plan, prm, km, vm, stream);
     }
   }
   switch (plan.heads_per_cta) {
     case 8:
-      return a.q_len > 1 ? launch_g<8, true>(a, plan, prm, km, vm, stream)
-                         : launch_g<8, false>(a, plan, prm, km, vm, stream);
+      return a.q_len > 1 ? launch_g<8, true, false, true>(a, plan, prm, km, vm, stream)
+                         : launch_g<8, false, false, true>(a, plan, prm, km, vm, stream);
     case 4:
-      return a.q_len > 1 ? launch_g<4, true>(a, plan, prm, km, vm, stream)
-                         : launch_g<4, false>(a, plan, prm, km, vm, stream);
+      return a.q_len > 1 ? launch_g<4, true, false, true>(a, plan, prm, km, vm, stream)
+                         : launch_g<4, false, false, true>(a, plan, prm, km, vm, stream);
     case 2:
-      return a.q_len > 1 ? launch_g<2, true>(a, plan, prm, km, vm, stream)
-                         : launch_g<2, false>(a, plan, prm, km, vm, stream);
+      return a.q_len > 1 ? launch_g<2, true, false, true>(a, plan, prm, km, vm, stream)
+                         : launch_g<2, false, false, true>(a, plan, prm, km, vm, stream);
     default:
-      return a.q_len > 1 ? launch_g<1, true>(a, plan, prm, km, vm, stream)
-                         : launch_g<1, false>(a, plan, prm, km, vm, stream);
+      return a.q_len > 1 ? launch_g<1, true, false, true>(a, plan, prm, km, vm, stream)
+                         : launch_g<1, false, false, true>(a, plan, prm, km, vm, stream);
   }
 }
 
