@@ -384,7 +384,7 @@ def run_gpu(args, world, rank):
         "kv_tokens_per_s": round(kv_tps, 1),
         "pct_of_peak_hbm": round(100 * value / hbm_peak, 2),
         "gpu_launches": K,
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel (store fused)",
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_kernel (bf16, producer warp, store fused)",
                      "achieved": round(dec_gbs, 1), "peak": hbm_peak,
                      "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
                      "frac": round(dec_gbs / hbm_peak, 4),
@@ -915,21 +915,23 @@ def run_shared_prefix_profile(args):
 
 def run_fp8_decode_profile(args, long_ctx: bool, fused_store: bool = False):
     """Small-footprint FP8 decode run for ncu: the decode-b64 shapes (2 query
-    heads per kv head) or, with `long_ctx`, 8 sequences of 32k-64k tokens with
-    4 query heads per kv head; pools quantized once with kv_cache_store_fp8.
+    heads per kv head) or, with `long_ctx`, the first 2 sequences of
+    long-decode-b8 (4 query heads per kv head) with the 37 splits the planner
+    picks for the full batch, as run_long_decode_profile; pools quantized once
+    with kv_cache_store_fp8.
     `fused_store`: the decode-b64 step's store of the new tokens and the decode
     in one launch (paged_decode_attention_fp8_store)."""
     from paged_kv_cache_214_gb300 import pkv
     dev = torch.device("cuda", torch.cuda.current_device())
     if long_ctx:
-        lens = W._uniform_ints(32768, 65536, 8, W.seed_for(5))
-        Hq, name = 32, "long-decode-b8-fp8-trimmed"
+        lens = W._uniform_ints(32768, 131072, 8, W.seed_for(5))[:2]
+        Hq, name, maxblk, splits = 32, "long-decode-b8-fp8-2seq", 512, 37
     else:
         lens = W._uniform_ints(512, 4096, 64, W.seed_for(2))
-        Hq, name = 16, "decode-b64-fp8"
+        Hq, name, maxblk, splits = 16, "decode-b64-fp8", None, 0
     nblk = sum(-(-L // W.BLOCK_SIZE) for L in lens)
     w = W.make_decode(lens, Hq, 8, nblk, W.seed_for(2), name=name,
-                      store_new_token=fused_store, pool_device=dev)
+                      store_new_token=fused_store, pool_device=dev, max_blocks_per_seq=maxblk)
     k8 = torch.empty((nblk, w.block_size, w.Hkv, w.D), dtype=torch.uint8, device=dev)
     v8 = torch.empty_like(k8)
     ks = vs = 6.0 / 448
@@ -940,7 +942,8 @@ def run_fp8_decode_profile(args, long_ctx: bool, fused_store: bool = False):
     q, tables, ctx = w.q.to(dev), w.block_tables.to(dev), w.context_lens.to(dev)
     out = torch.empty_like(q)
     lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
-    need = pkv.paged_decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, tables.shape[1])
+    need = pkv.paged_decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, tables.shape[1],
+                                            num_splits=splits)
     ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -950,11 +953,12 @@ def run_fp8_decode_profile(args, long_ctx: bool, fused_store: bool = False):
         def call():
             pkv.paged_decode_attention_fp8_store(q, kn, vn, slots, k8, v8, tables, ctx, w.scale,
                                                  ks, vs, out=out, lse=lse, workspace=ws,
-                                                 stream=stream)
+                                                 num_splits=splits, stream=stream)
     else:
         def call():
             pkv.paged_decode_attention_fp8(q, k8, v8, tables, ctx, w.scale, ks, vs, out=out,
-                                           lse=lse, workspace=ws, stream=stream)
+                                           lse=lse, workspace=ws, num_splits=splits,
+                                           stream=stream)
     for _ in range(args.warmup):
         call()
     med, _ = _time_calls(call, args.steps, stream)
