@@ -163,10 +163,12 @@ __device__ __forceinline__ void merge_row(const float* lrow, const float* orow, 
 // holds 16 KB; without a producer warp, 4 stages (64 KB) let three blocks
 // share an SM and warps 0 and 1 issue the K and the V copy of each stage;
 // with one (kProd), 6 stages at two blocks per SM (the fifth warp's registers
-// leave no room for a third block).
+// leave no room for a third block).  bf16 without a producer warp (batches
+// split into 64-token tiles, one or a few per block): 2 stages, three blocks
+// per SM, so that all of such a batch's blocks are resident at once.
 template <bool kFp8, bool kProd = false>
 struct Geo {
-  static constexpr int kStagesN = kFp8 ? (kProd ? 6 : 4) : 3;
+  static constexpr int kStagesN = kFp8 ? (kProd ? 6 : 4) : (kProd ? 3 : 2);
   static constexpr int kOpBytes = kTile * (kFp8 ? 128 : 256);  // one of K or V for a stage
   static constexpr int kStageB = 2 * kOpBytes;
   static constexpr int kIssuers = kFp8 ? 2 : 4;
@@ -438,7 +440,7 @@ __device__ __forceinline__ void store_new_row(const DecodeParams& p, int b, int 
 // release a stage before its next tile.  One kv head per block; G of its
 // query heads.
 template <int G, bool kMQ, bool kFp8, bool kProd>
-__global__ void __launch_bounds__(kProd ? kThreads + 32 : kThreads, 2)
+__global__ void __launch_bounds__(kProd ? kThreads + 32 : kThreads, kProd ? 2 : 3)
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
   using L = SmemLayout<G, kFp8, kProd>;
@@ -1025,6 +1027,24 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
       default:
         return prod ? launch_g<1, false, true, true>(a, plan, prm, km, vm, stream)
                     : launch_g<1, false, true, false>(a, plan, prm, km, vm, stream);
+    }
+  }
+  // bf16 batches split into 64-token tiles: the 2-stage consumer-issued form
+  // (three blocks per SM)
+  if (plan.split_tokens < kBlockSize) {
+    switch (plan.heads_per_cta) {
+      case 8:
+        return a.q_len > 1 ? launch_g<8, true, false, false>(a, plan, prm, km, vm, stream)
+                           : launch_g<8, false, false, false>(a, plan, prm, km, vm, stream);
+      case 4:
+        return a.q_len > 1 ? launch_g<4, true, false, false>(a, plan, prm, km, vm, stream)
+                           : launch_g<4, false, false, false>(a, plan, prm, km, vm, stream);
+      case 2:
+        return a.q_len > 1 ? launch_g<2, true, false, false>(a, plan, prm, km, vm, stream)
+                           : launch_g<2, false, false, false>(a, plan, prm, km, vm, stream);
+      default:
+        return a.q_len > 1 ? launch_g<1, true, false, false>(a, plan, prm, km, vm, stream)
+                           : launch_g<1, false, false, false>(a, plan, prm, km, vm, stream);
     }
   }
   switch (plan.heads_per_cta) {
