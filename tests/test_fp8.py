@@ -193,6 +193,17 @@ def test_decode_forced_splits(num_splits):
     run_decode_and_check(w, *SCALES[1], num_splits=num_splits, what=f"splits={num_splits}")
 
 
+@pytest.mark.parametrize("num_splits,Hq", [(2, 16), (3, 32), (2, 64)])
+def test_decode_long_splits(num_splits, Hq):
+    # splits of 8 blocks or more run the E4M3 decode's producer-warp form (a
+    # fifth warp copies the stages, 6 stages at two blocks per SM)
+    w = W.make_decode(CTX, Hq, 8, 64, 8450 + Hq + num_splits)
+    maxblk = w.block_tables.shape[1]
+    S = pkv.paged_decode_num_splits(w.B, w.Hq, w.Hkv, w.D, maxblk, w.block_size, num_splits)
+    assert S == num_splits and -(-maxblk // S) >= 8
+    run_decode_and_check(w, *SCALES[1], num_splits=num_splits, what=f"long splits S={S}")
+
+
 def test_decode_empty_context_gives_zero_and_minus_inf():
     w = W.make_decode([0, 300, 0], 16, 8, 8, 8500)
     run_decode_and_check(w, *SCALES[1], what="empty contexts")
@@ -209,9 +220,11 @@ def test_decode_b64_workload():
     run_decode_and_check(w, *SCALES[1], what="decode-b64 fp8")
 
 
+@pytest.mark.parametrize("num_splits", [0, 2])
 @pytest.mark.parametrize("Hq,Hkv", [(16, 8), (32, 8), (64, 8)])
-def test_fused_store_decode_same_bits_as_two_calls(Hq, Hkv):
+def test_fused_store_decode_same_bits_as_two_calls(Hq, Hkv, num_splits):
     # paged_decode_attention_fp8_store = kv_cache_store_fp8 + the E4M3 decode
+    # (num_splits = 2: 12-block splits, the producer-warp form)
     dev = "cuda"
     ks, vs = SCALES[1]
     w = W.make_decode([0, 3, 256, 257, 1000, 3000, 6000], Hq, Hkv, 64, 8700 + Hq)
@@ -222,12 +235,13 @@ def test_fused_store_decode_same_bits_as_two_calls(Hq, Hkv):
     q, kn, vn, slots = w.q.to(dev), w.k_new.to(dev), w.v_new.to(dev), w.slot_mapping.to(dev)
     tables, ctx = w.block_tables.to(dev), w.context_lens.to(dev)
     pkv.kv_cache_store_fp8(kn, vn, k8, v8, slots, ks, vs)
-    o1, l1 = pkv.paged_decode_attention_fp8(q, k8, v8, tables, ctx, w.scale, ks, vs)
+    o1, l1 = pkv.paged_decode_attention_fp8(q, k8, v8, tables, ctx, w.scale, ks, vs,
+                                            num_splits=num_splits)
     o2, l2 = pkv.paged_decode_attention_fp8_store(q, kn, vn, slots, k8b, v8b, tables, ctx,
-                                                  w.scale, ks, vs)
+                                                  w.scale, ks, vs, num_splits=num_splits)
     torch.cuda.synchronize()
     assert pkv.get_device_error() == pkv.PKV_OK
     assert torch.equal(k8, k8b) and torch.equal(v8, v8b)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
     # and the oracle agrees with the fused result
-    run_decode_and_check(w, ks, vs, what=f"fused fp8 Hq={Hq}")
+    run_decode_and_check(w, ks, vs, num_splits=num_splits, what=f"fused fp8 Hq={Hq}")

@@ -60,6 +60,41 @@ def test_decode_wait_runs_out_then_recovers(wait_fault, num_splits):
     assert_close(out, lse, ref_o, ref_l, f"decode after a timeout, S={num_splits}")
 
 
+@pytest.mark.parametrize("num_splits", [0, 2])
+def test_fp8_decode_wait_runs_out_then_recovers(wait_fault, num_splits):
+    # E4M3 pools: the consumer-issued form (automatic splits of this batch) and
+    # the producer-warp form (num_splits = 2: splits of 8 blocks or more).  After
+    # the timeout the next call must return PKV_OK with the bits of a call made
+    # before the fault (the E4M3 decode is checked against the oracle in
+    # test_fp8.py).
+    w = W.make_decode([3000, 1500, 3500, 4000], 32, 8, 64, 8150 + num_splits,
+                      store_new_token=False)
+    dev = "cuda"
+    NB, bs = w.num_blocks, w.block_size
+    k8 = torch.empty((NB, bs, w.Hkv, w.D), dtype=torch.uint8, device=dev)
+    v8 = torch.empty_like(k8)
+    every = torch.arange(NB * bs, dtype=torch.int32, device=dev)
+    ks = vs = 6.0 / 448
+    pkv.kv_cache_store_fp8(w.k_cache.to(dev).view(-1, w.Hkv, w.D),
+                           w.v_cache.to(dev).view(-1, w.Hkv, w.D), k8, v8, every, ks, vs)
+    args = (w.q.to(dev), k8, v8, w.block_tables.to(dev), w.context_lens.to(dev), w.scale, ks, vs)
+    ref_o, ref_l = pkv.paged_decode_attention_fp8(*args, num_splits=num_splits)
+    ref_o, ref_l = ref_o.clone(), ref_l.clone()
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == pkv.PKV_OK
+    wait_fault(2)
+    t0 = time.perf_counter()
+    pkv.paged_decode_attention_fp8(*args, num_splits=num_splits)
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 10.0
+    assert pkv.get_device_error() == pkv.PKV_ERR_TIMEOUT
+    pkv.testing_set_wait_fault(0, -1)
+    out, lse = pkv.paged_decode_attention_fp8(*args, num_splits=num_splits)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == pkv.PKV_OK
+    assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
+
+
 @pytest.mark.parametrize("Hq,Hkv", [(16, 8), (8, 8)])
 def test_prefill_wait_runs_out_then_recovers(wait_fault, Hq, Hkv):
     w = W.make_prefill([512, 300, 0], [256, 300, 640], Hq, Hkv, 32, 8200 + Hq)
