@@ -614,22 +614,42 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
         rowa = static_cast<int64_t>(e.q_begin + e.q0 + ra) * p.Hq + e.h;
         rowb = static_cast<int64_t>(e.q_begin + e.q0 + rb) * p.Hq + e.h;
       }
-#pragma unroll 1
-      for (int h2 = 0; h2 < 2; ++h2) {   // dims [64 h2, 64 h2 + 64): box h2 of the row
-        uint32_t o[32];
-        tmem_ld16x256_x8_wait(o_col + h2 * 64, o);
+      // O for both rows in one load: o[4j], o[4j+1] (row ra) and o[4j+2],
+      // o[4j+3] (row rb) hold dims 8j + 2 m4 + {0, 1}, j = 0..15.  Lanes m4 and
+      // m4 ^ 1 swap one pair per 16-dim group, so that each lane writes 4
+      // consecutive dims and the four lanes of a row one whole 32-byte sector
+      // per store (fp32 partials: two sectors): even lanes keep group j = 2i
+      // (dims 16i + 2 m4 ..), odd lanes j = 2i + 1 (dims 16i + 8 + 2 (m4 - 1) ..).
+      uint32_t o[64];
+      tmem_ld16x256_x16_wait(o_col, o);
+      const bool odd = m4 & 1;
+      const int cbase = odd ? 8 + 2 * (m4 - 1) : 2 * m4;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int col = 64 * h2 + 8 * j + 2 * m4;
-          const float a0 = __uint_as_float(o[4 * j]) * ia, a1 = __uint_as_float(o[4 * j + 1]) * ia;
-          const float b0 = __uint_as_float(o[4 * j + 2]) * ib, b1 = __uint_as_float(o[4 * j + 3]) * ib;
-          if constexpr (kPrefix) {
-            if (va) *reinterpret_cast<float2*>(p.part_o + rowa * kHeadDim + col) = make_float2(a0, a1);
-            if (vb) *reinterpret_cast<float2*>(p.part_o + rowb * kHeadDim + col) = make_float2(b0, b1);
-          } else {
-            if (va) *reinterpret_cast<uint32_t*>(p.out + rowa * kHeadDim + col) = pack_bf16x2(a0, a1);
-            if (vb) *reinterpret_cast<uint32_t*>(p.out + rowb * kHeadDim + col) = pack_bf16x2(b0, b1);
-          }
+      for (int i = 0; i < 8; ++i) {
+        const int col = 16 * i + cbase;
+        const float ae0 = __uint_as_float(o[8 * i]) * ia, ae1 = __uint_as_float(o[8 * i + 1]) * ia;
+        const float be0 = __uint_as_float(o[8 * i + 2]) * ib, be1 = __uint_as_float(o[8 * i + 3]) * ib;
+        const float ao0 = __uint_as_float(o[8 * i + 4]) * ia, ao1 = __uint_as_float(o[8 * i + 5]) * ia;
+        const float bo0 = __uint_as_float(o[8 * i + 6]) * ib, bo1 = __uint_as_float(o[8 * i + 7]) * ib;
+        if constexpr (kPrefix) {
+          // send the pair the neighbour keeps; keep own pair first (even) or second (odd)
+          const float sa0 = odd ? ae0 : ao0, sa1 = odd ? ae1 : ao1;
+          const float sb0 = odd ? be0 : bo0, sb1 = odd ? be1 : bo1;
+          const float xa0 = __shfl_xor_sync(kFull, sa0, 1), xa1 = __shfl_xor_sync(kFull, sa1, 1);
+          const float xb0 = __shfl_xor_sync(kFull, sb0, 1), xb1 = __shfl_xor_sync(kFull, sb1, 1);
+          const float4 va4 = odd ? make_float4(xa0, xa1, ao0, ao1) : make_float4(ae0, ae1, xa0, xa1);
+          const float4 vb4 = odd ? make_float4(xb0, xb1, bo0, bo1) : make_float4(be0, be1, xb0, xb1);
+          if (va) *reinterpret_cast<float4*>(p.part_o + rowa * kHeadDim + col) = va4;
+          if (vb) *reinterpret_cast<float4*>(p.part_o + rowb * kHeadDim + col) = vb4;
+        } else {
+          const uint32_t ae = pack_bf16x2(ae0, ae1), ao = pack_bf16x2(ao0, ao1);
+          const uint32_t be = pack_bf16x2(be0, be1), bo = pack_bf16x2(bo0, bo1);
+          const uint32_t xa = __shfl_xor_sync(kFull, odd ? ae : ao, 1);
+          const uint32_t xb = __shfl_xor_sync(kFull, odd ? be : bo, 1);
+          const uint2 wa = odd ? make_uint2(xa, ao) : make_uint2(ae, xa);
+          const uint2 wb = odd ? make_uint2(xb, bo) : make_uint2(be, xb);
+          if (va) *reinterpret_cast<uint2*>(p.out + rowa * kHeadDim + col) = wa;
+          if (vb) *reinterpret_cast<uint2*>(p.out + rowb * kHeadDim + col) = wb;
         }
       }
       if (m4 == 0) {
