@@ -115,3 +115,23 @@ def test_noalloc_refuses_a_bad_argument_before_queueing_anything():
     out, lse = _noalloc(w, args, 2)
     assert_close(out, lse, *_oracle(w), "after a refused call")
     assert np.isfinite(lse.cpu().numpy()).all()
+
+
+def test_noalloc_after_a_timed_out_call():
+    """A no-allocation call whose wait runs out (the test hook lowers the wait
+    limit and withholds a tile; nothing faults or hangs) reports
+    PKV_ERR_TIMEOUT, and the next call, on the same shared scratch, returns
+    PKV_OK and matches the oracle."""
+    w = W.make_decode([3000, 1500, 3500], 16, 8, 48, 7400, store_new_token=False)
+    args = _inputs(w)
+    out = torch.zeros_like(args[0])
+    assert pkv.get_device_error() == pkv.PKV_OK
+    try:
+        pkv.testing_set_wait_fault(1_000_000, 2)
+        pkv.paged_decode_attention_noalloc(*args, w.scale, out, num_splits=4)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == pkv.PKV_ERR_TIMEOUT
+    finally:
+        pkv.testing_set_wait_fault(0, -1)
+    o, lse = _noalloc(w, args, 4)
+    assert_close(o, lse, *_oracle(w), "no-allocation call after a timed-out one")
