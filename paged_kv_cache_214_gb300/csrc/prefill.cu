@@ -23,6 +23,7 @@
 //   warp 10 (MMA)  S_t = Q K_t^T into one of three S buffers in tensor memory.
 //   warp 11 (MMA)  O += P_t V_t, A = P_t read from tensor memory, B = V_t
 //                  MN-major straight from its TMA tile.
+// (Causal prefill with an even group size uses the head-pair kernel below.)
 //   warps 0-7      softmax: warp w owns 16 whole rows of every S tile (half of
 //                  its TMEM lane quarter, read with the 16-lane access shapes),
 //                  keeps the running max in base 2, rescales O only when the
@@ -31,10 +32,11 @@
 //                  first 64 columns of the tile's S buffer.  No softmax warp
 //                  waits for another, so the exp2 work of one overlaps the
 //                  loads and reductions of the other on the same SM quarter.
-// The MMAs come from two threads: one thread issuing M=N=128 tcgen05.mma in a
-// chain waits ~116 cycles per instruction, about half the tensor pipe, while
-// two independent chains fill it.  S is triple-buffered, so the S of tile t+1
-// (and t+2) is computed while the softmax of tile t runs.
+// The MMAs come from two warps, each running its issue loop with all lanes and
+// issuing through one elected lane (issuing from a lone lane-0 branch cost
+// ~116 cycles per M=N=128 product, about half the tensor pipe).  S is
+// triple-buffered, so the S of tile t+1 (and t+2) is computed while the
+// softmax of tile t runs.
 // TMEM (512 columns): S_0 | S_1 | S_2 | O.
 // K and V each have three 32 KB stages (Q one buffer).  The tensor copies of
 // one thread complete one after another, so every tile copy is split in its
@@ -469,7 +471,8 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
     if (!ok && lane == 0) flags[0] = 1;
   } else if (warp == kSWarp) {
     // ------------------------------------------------------------ MMA: S = Q K^T
-    if (lane == 0) {
+    // (the whole warp runs the loop and waits; an elected lane issues)
+    {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kM, kN, 0);   // B = K, K-major
       bool ok = true, timeout = false;
       int gi = 0, gk = 0;
@@ -482,13 +485,13 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
         int k2 = k + 1;
         Item nx;
         const bool have_next = next_item<kMode>(p, n_rounds, k2, nx, false);
-        if (!mbar_wait(bar(kBarQFull), gi & 1)) { ok = false; timeout = true; break; }
+        if (!warp_wait(bar(kBarQFull), gi & 1)) { ok = false; timeout = true; break; }
         const uint32_t q_s = sbase + kOffQ;
         for (int kt = 0; kt < it.n; ++kt, ++gk, sb.next(), rk.next()) {
-          if (flags[0]) { ok = false; break; }
-          if (!mbar_wait(bar(kBarKFull + rk.idx), rk.ph)) { ok = false; timeout = true; break; }
+          if (__any_sync(kFull, flags[0] != 0)) { ok = false; break; }
+          if (!warp_wait(bar(kBarKFull + rk.idx), rk.ph)) { ok = false; timeout = true; break; }
           // S buffer free: the PV that read P from it (three tiles back) is done
-          if (gk >= kSBufs && !mbar_wait(bar(kBarPVDone + sb.idx), sb.ph ^ 1u)) {
+          if (gk >= kSBufs && !warp_wait(bar(kBarPVDone + sb.idx), sb.ph ^ 1u)) {
             ok = false;
             timeout = true;
             break;
@@ -499,28 +502,28 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
-            umma_bf16(d_s, smem_desc_sw128(q_s + off, 16, 1024),
-                      smem_desc_sw128(k_s + off, 16, 1024), idesc_s, ks > 0);
+            umma_bf16_warp(d_s, smem_desc_sw128(q_s + off, 16, 1024),
+                           smem_desc_sw128(k_s + off, 16, 1024), idesc_s, ks > 0);
           }
-          umma_commit(bar(kBarSFull + sb.idx));
-          umma_commit(bar(kBarKEmpty + rk.idx));
+          umma_commit_warp(bar(kBarSFull + sb.idx));
+          umma_commit_warp(bar(kBarKEmpty + rk.idx));
         }
         if (!ok) break;
-        umma_commit(bar(kBarQEmpty));
+        umma_commit_warp(bar(kBarQEmpty));
         ++gi;
         it = nx;
         k = k2;
         have = have_next;
       }
-      if (timeout) record_error(p.err, kErrTimeout);
-      if (!ok) flags[0] = 1;
-      // every MMA this thread issued has completed once this arrives
-      umma_commit(bar(kBarDrainS));
-      (void)mbar_wait(bar(kBarDrainS), 0);
+      if (timeout && lane == 0) record_error(p.err, kErrTimeout);
+      if (!ok && lane == 0) flags[0] = 1;
+      // every MMA this warp issued has completed once this arrives
+      umma_commit_warp(bar(kBarDrainS));
+      (void)warp_wait(bar(kBarDrainS), 0);
     }
   } else if (warp == kPVWarp) {
     // ------------------------------------------------------------ MMA: O += P V
-    if (lane == 0) {
+    {
       constexpr uint32_t idesc_o = idesc_bf16_f32(kM, kHeadDim, 1);  // B = V, MN-major
       bool ok = true, timeout = false;
       int gk = 0;
@@ -535,9 +538,9 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
         Item nx;
         const bool have_next = next_item<kMode>(p, n_rounds, k2, nx, false);
         for (int kt = 0; kt < it.n; ++kt, ++gk, sb.next(), rv.next()) {
-          if (flags[0]) { ok = false; break; }
-          if (!mbar_wait(bar(kBarVFull + rv.idx), rv.ph) ||
-              !mbar_wait(bar(kBarPFull + sb.idx), sb.ph)) {
+          if (__any_sync(kFull, flags[0] != 0)) { ok = false; break; }
+          if (!warp_wait(bar(kBarVFull + rv.idx), rv.ph) ||
+              !warp_wait(bar(kBarPFull + sb.idx), sb.ph)) {
             ok = false;
             timeout = true;
             break;
@@ -549,22 +552,22 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
           for (int ks = 0; ks < 8; ++ks) {
             // A = P: 16 keys = 8 packed columns per step.  B = V: 64-dim boxes
             // kHalf apart (LBO), 8-key swizzle atoms 1024 bytes apart (SBO).
-            umma_bf16_tmem_a(d_o, p_t + ks * 8, smem_desc_sw128(v_s + ks * 2048, kHalf, 1024),
-                             idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
+            umma_bf16_tmem_a_warp(d_o, p_t + ks * 8, smem_desc_sw128(v_s + ks * 2048, kHalf, 1024),
+                                  idesc_o, (kt > 0 || ks > 0) ? 1u : 0u);
           }
-          umma_commit(bar(kBarVEmpty + rv.idx));
-          umma_commit(bar(kBarPVDone + sb.idx));
+          umma_commit_warp(bar(kBarVEmpty + rv.idx));
+          umma_commit_warp(bar(kBarPVDone + sb.idx));
         }
         if (!ok) break;
-        umma_commit(bar(kBarOFull));
+        umma_commit_warp(bar(kBarOFull));
         it = nx;
         k = k2;
         have = have_next;
       }
-      if (timeout) record_error(p.err, kErrTimeout);
-      if (!ok) flags[0] = 1;
-      umma_commit(bar(kBarDrainPV));
-      (void)mbar_wait(bar(kBarDrainPV), 0);
+      if (timeout && lane == 0) record_error(p.err, kErrTimeout);
+      if (!ok && lane == 0) flags[0] = 1;
+      umma_commit_warp(bar(kBarDrainPV));
+      (void)warp_wait(bar(kBarDrainPV), 0);
     }
   } else {
     // ------------------------------------------------------------ softmax
