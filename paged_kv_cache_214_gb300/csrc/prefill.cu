@@ -23,7 +23,6 @@
 //   warp 10 (MMA)  S_t = Q K_t^T into one of three S buffers in tensor memory.
 //   warp 11 (MMA)  O += P_t V_t, A = P_t read from tensor memory, B = V_t
 //                  MN-major straight from its TMA tile.
-// (Causal prefill with an even group size uses the head-pair kernel below.)
 //   warps 0-7      softmax: warp w owns 16 whole rows of every S tile (half of
 //                  its TMEM lane quarter, read with the 16-lane access shapes),
 //                  keeps the running max in base 2, rescales O only when the
@@ -145,9 +144,7 @@ struct Item {
   const int32_t* table;
 };
 
-// kHeads: query heads per causal item (1, or 2 for the head-pair kernel: heads
-// h, h + 1 of one kv head, h even).
-template <int kMode, int kHeads = 1>
+template <int kMode>
 __device__ __forceinline__ Item get_item(const PrefillParams& p, int idx, bool report) {
   Item it;
   const int g = p.Hq / p.Hkv;
@@ -190,12 +187,11 @@ __device__ __forceinline__ Item get_item(const PrefillParams& p, int idx, bool r
     it.Lk = p.prefix_tokens;
     it.table = p.block_tables;
   } else {
-    const int hpi = p.Hq / kHeads;             // items per (row tile, sequence)
-    const int per_lvl = p.B * hpi;
+    const int per_lvl = p.B * p.Hq;
     const int lvl = idx / per_lvl;             // heavier (later) row tiles first
     const int rem = idx - lvl * per_lvl;
-    const int b = rem / hpi;
-    it.h = (rem - b * hpi) * kHeads;
+    const int b = rem / p.Hq;
+    it.h = rem - b * p.Hq;
     it.kvh = it.h / g;
     it.q_begin = p.cu_q[b];
     const int Lq = p.cu_q[b + 1] - it.q_begin;
@@ -227,13 +223,13 @@ __device__ __forceinline__ int item_index(int k) {
 }
 
 // First non-empty item at or after round k (k is advanced to it).
-template <int kMode, int kHeads = 1>
+template <int kMode>
 __device__ __forceinline__ bool next_item(const PrefillParams& p, int n_rounds, int& k, Item& it,
                                           bool report) {
   for (; k < n_rounds; ++k) {
     const int idx = item_index(k);
     if (idx >= p.n_items) continue;
-    it = get_item<kMode, kHeads>(p, idx, report);
+    it = get_item<kMode>(p, idx, report);
     if (it.n > 0) return true;
   }
   return false;
@@ -835,626 +831,6 @@ paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
 }
 
 
-// ------------------------------------------------------------------ head pairs
-// Causal prefill with two query heads per item (h, h + 1 of one kv head, for
-// an even group size g = Hq / Hkv): both heads' products read the same staged
-// K and V tiles, so each tile crosses from L2 once per pair instead of once per
-// head, and one MMA thread interleaves the two heads so that the softmax of one
-// runs while the tensor pipe works for the other:
-//     S_a(t)  PV_b(t-1)  S_b(t)  PV_a(t)  S_a(t+1)  PV_b(t)  ...
-// The softmax of head a for tile t has the time of PV_b(t-1) and S_b(t) to
-// finish before PV_a(t) needs its P, and the same holds for head b.
-// TMEM (512 columns): S_a | S_b | O_a | O_b; P overwrites the first 64 columns
-// of its head's S, so the next S of a head is issued once the PV that reads P
-// has completed (products with different accumulators are not ordered).
-// Splitting S into two N = 64 halves, to issue the half that P does not use
-// early, measured slower: an N = 64 product reads as many A bytes from shared
-// memory as an N = 128 one, and the two halves exceed its read bandwidth.
-// Sixteen warps, as four warpgroups whose register shares are moved with
-// setmaxnreg (launched at 128 per thread: softmax 168, output 72, the rest 104;
-// 2 x 128 x 168 + 128 x 72 + 128 x 104 = all 65,536 launched):
-//   warps 0-3   softmax of head a, warps 4-7 of head b: a thread owns one
-//               row (its TMEM lane) and holds the row's 128 S values, so the
-//               row max and sum need no shuffles; at the end of an item the
-//               warps also write lse and 1 / l per row
-//   warps 8-11  output: once an item's last PV of a head has completed, read O
-//               (a thread per row of the warp's lane quarter), hand the
-//               accumulator back to the next item, normalise and write
-//   warp 12     TMA: Q of both heads (one buffer each) and K tiles
-//   warp 13     TMA: V tiles
-//   warp 14     lane 0 issues every MMA
-//   warp 15     idle
-namespace hp {
-constexpr int kThreads = 16 * 32;
-constexpr int kRegsLaunch = 128;   // 65,536 / kThreads
-constexpr int kRegsSoftmax = 168;
-constexpr int kRegsOut = 72;
-constexpr int kRegsRest = 104;
-static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOut + 128 * kRegsRest <= kThreads * kRegsLaunch,
-              "warpgroup register shares exceed the launch's registers");
-constexpr int kOutWarp = 8;
-constexpr int kQKWarp = 12;
-constexpr int kVWarp = 13;
-constexpr int kMmaWarp = 14;
-constexpr int kKStages = 3;
-constexpr int kVStages = 2;
-constexpr int kOffQ = 0;                           // [head]
-constexpr int kOffK = kOffQ + 2 * kTile;           // [stage]
-constexpr int kOffV = kOffK + kKStages * kTile;    // [stage]
-constexpr int kOffInvL = kOffV + kVStages * kTile; // [head][row] 1 / l of the finished item
-// barriers
-constexpr int kBQFull = 0;                         // [head]
-constexpr int kBQEmpty = 2;                        // [head]
-constexpr int kBKFull = 4;                         // [stage]
-constexpr int kBKEmpty = kBKFull + kKStages;       // [stage]
-constexpr int kBVFull = kBKEmpty + kKStages;       // [stage]
-constexpr int kBVEmpty = kBVFull + kVStages;       // [stage]
-constexpr int kBSFull = kBVEmpty + kVStages;       // [head]
-constexpr int kBPFull = kBSFull + 2;               // [head], the head's 4 softmax warps
-constexpr int kBPVDone = kBPFull + 2;              // [head]
-constexpr int kBOFull = kBPVDone + 2;              // [head]: an item's last PV completed
-constexpr int kBOFree = kBOFull + 2;               // [head], 4 output warps: O read
-constexpr int kBLFull = kBOFree + 2;               // [head], the head's 4 softmax warps: 1 / l written
-constexpr int kBLFree = kBLFull + 2;               // [head], 4 output warps: 1 / l read
-constexpr int kBDrain = kBLFree + 2;
-constexpr int kNumBars = kBDrain + 1;
-constexpr int kOffBars = kOffInvL + 2 * kM * 4;
-constexpr int kOffTmem = kOffBars + kNumBars * 8;
-constexpr int kOffFlags = kOffTmem + 8;
-constexpr int kSmemBytes = kOffFlags + 32 + 1024;
-static_assert(kSmemBytes <= 227 * 1024, "one block per SM must fit in shared memory");
-static_assert(2 * kKStages + 4 <= 32 && 2 * kVStages <= 32, "lanes of the copy issuers");
-constexpr uint32_t kColS = 0;     // + 128 * head
-constexpr uint32_t kColO = 256;   // + 128 * head
-}  // namespace hp
-
-__global__ void __launch_bounds__(hp::kThreads, 1)
-paged_prefill_pair_kernel(const __grid_constant__ CUtensorMap qmap,
-                          const __grid_constant__ CUtensorMap kmap,
-                          const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
-  using hp::kOutWarp;
-  using hp::kQKWarp;
-  using hp::kVWarp;
-  using hp::kMmaWarp;
-  using hp::kKStages;
-  using hp::kVStages;
-  using hp::kOffQ;
-  using hp::kOffK;
-  using hp::kOffV;
-  using hp::kOffInvL;
-  using hp::kBQFull;
-  using hp::kBQEmpty;
-  using hp::kBKFull;
-  using hp::kBKEmpty;
-  using hp::kBVFull;
-  using hp::kBVEmpty;
-  using hp::kBSFull;
-  using hp::kBPFull;
-  using hp::kBPVDone;
-  using hp::kBOFull;
-  using hp::kBOFree;
-  using hp::kBLFull;
-  using hp::kBLFree;
-  using hp::kBDrain;
-  using hp::kNumBars;
-  using hp::kOffBars;
-  using hp::kOffTmem;
-  using hp::kOffFlags;
-  using hp::kColS;
-  using hp::kColO;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sbase = smem_addr(smem);
-  const uint32_t bars = sbase + kOffBars;
-  auto bar = [&](int i) { return bars + 8u * i; };
-  volatile int* flags = reinterpret_cast<volatile int*>(smem + kOffFlags);
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + kOffTmem);
-  float* inv_l = reinterpret_cast<float*>(smem + kOffInvL);
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const int n_rounds = (p.n_items + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
-
-  if (tid == 0) {
-    for (int i = 0; i < kNumBars; ++i) {
-      uint32_t count = 1;
-      if ((i >= kBPFull && i < kBPFull + 2) || (i >= kBLFull && i < kBLFull + 2))
-        count = 4;   // a head's softmax warps
-      if ((i >= kBOFree && i < kBOFree + 2) || (i >= kBLFree && i < kBLFree + 2))
-        count = 4;   // output warps
-      mbar_init(bar(i), count);
-    }
-    for (int i = 0; i < 8; ++i) flags[i] = 0;   // abort, K / V tiles issued, Q loads per head
-    fence_barrier_init();
-  }
-  if (warp == kMmaWarp) {
-    tmem_alloc(sbase + kOffTmem, 512);
-    tmem_relinquish();
-  }
-  if (warp == kQKWarp && lane == 0) {
-    tma_prefetch_map(&qmap);
-    tma_prefetch_map(&kmap);
-  }
-  if (warp == kVWarp && lane == 0) tma_prefetch_map(&vmap);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  // End of every warpgroup's work (each returns from its own branch, so that
-  // no code runs under two register shares; each warpgroup sets its share at
-  // one place, first thing): after an abort, wait (bounded) for TMA
-  // copies that may still be landing, then free the tensor memory.
-  auto finish = [&]() {
-    tc_fence_before();
-    named_barrier(1, hp::kThreads);
-    if (flags[0] && tid == kQKWarp * 32) {
-      const int kin = flags[1];
-      for (int x = max(0, kin - kKStages); x < kin; ++x)
-        (void)mbar_wait(bar(kBKFull + x % kKStages), (x / kKStages) & 1);
-      for (int hh = 0; hh < 2; ++hh) {
-        const int qin = flags[3 + hh];
-        if (qin > 0) (void)mbar_wait(bar(kBQFull + hh), (qin - 1) & 1);
-      }
-    }
-    if (flags[0] && tid == kVWarp * 32) {
-      const int vin = flags[2];
-      for (int x = max(0, vin - kVStages); x < vin; ++x)
-        (void)mbar_wait(bar(kBVFull + x % kVStages), (x / kVStages) & 1);
-    }
-    named_barrier(1, hp::kThreads);
-    if (warp == kMmaWarp) {
-      tc_fence_after();
-      tmem_dealloc(tmem, 512);
-    }
-  };
-
-  if (warp < kOutWarp) {
-    // ------------------------------------------------------------ softmax
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(hp::kRegsSoftmax));
-    // Warpgroup hh (warps 4 hh .. 4 hh + 3) takes head hh; thread t of warp w
-    // owns row r = 32 (w % 4) + t (its TMEM lane) and holds the row's 128 S
-    // values (the 32x32b access shape), so the row max and sum stay within the
-    // thread.  P overwrites the first half of those registers and goes back
-    // over the first 64 columns of the head's S: column c holds keys 2c, 2c + 1.
-    const int hh = warp >> 2;
-    const int row = (warp & 3) * 32 + lane;
-    const uint32_t lb = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const uint32_t s_col = lb + kColS + hh * kN;
-    const uint32_t o_col = lb + kColO + hh * kHeadDim;
-    const f32x2 sc2 = pack2(p.scale_log2, p.scale_log2);
-    bool ok = true, timeout = false;
-    int gi = 0, gk = 0;
-    Ring<kVStages> rv;   // V stage of the current tile (for the ragged-end clearing)
-    int k = 0;
-    Item it;
-    bool have = next_item<kCausal, 2>(p, n_rounds, k, it, warp == 0 && lane == 0);
-    while (have && ok) {
-      int k2 = k + 1;
-      Item nx;
-      const bool have_next = next_item<kCausal, 2>(p, n_rounds, k2, nx, warp == 0 && lane == 0);
-      const int vis = it.diag + row;   // last key this row sees
-      float m = -INFINITY;
-      f32x2 l2 = pack2(0.f, 0.f);      // running sum, as a pair
-      for (int kt = 0; kt < it.n; ++kt, ++gk, rv.next()) {
-        if (__any_sync(kFull, flags[0] != 0)) { ok = false; break; }
-        if (!(ok = warp_wait(bar(kBSFull + hh), gk & 1))) { timeout = true; break; }
-        tc_fence_after();
-        uint32_t s[128];
-        tmem_ld32x32b_x128_wait(s_col, s);
-        if (kt * kN + kN - 1 > it.diag) {   // causal edge
-          const int first_hidden = vis + 1 - kt * kN;   // columns >= this are hidden
-#pragma unroll
-          for (int j = 0; j < 128; ++j)
-            if (j >= first_hidden) s[j] = __float_as_uint(-INFINITY);
-        }
-        float x0 = __uint_as_float(s[0]), x1 = __uint_as_float(s[1]);
-        float x2 = __uint_as_float(s[2]), x3 = __uint_as_float(s[3]);
-#pragma unroll
-        for (int j = 4; j < 128; j += 4) {
-          x0 = fmaxf(x0, __uint_as_float(s[j]));
-          x1 = fmaxf(x1, __uint_as_float(s[j + 1]));
-          x2 = fmaxf(x2, __uint_as_float(s[j + 2]));
-          x3 = fmaxf(x3, __uint_as_float(s[j + 3]));
-        }
-        const float mt = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)) * p.scale_log2;
-        if (kt == 0) {
-          m = mt;
-        } else {
-          const bool need = mt > m + kLazyRescale;
-          if (__any_sync(kFull, need)) {
-            // the previous PV of this head must have finished accumulating into O
-            if (!(ok = warp_wait(bar(kBPVDone + hh), (gk - 1) & 1))) { timeout = true; break; }
-            tc_fence_after();
-            if (need) {
-              const float alpha = ex2(m - mt);
-              l2 = mul2(l2, pack2(alpha, alpha));
-              m = mt;
-#pragma unroll 1
-              for (int c = 0; c < kHeadDim; c += 8) {
-                uint32_t o[8];
-                tmem_ld32x32b_x8_wait(o_col + c, o);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-                tmem_st32x32b_x8(o_col + c, o);
-              }
-            }
-          }
-        }
-        // P = 2^(scale s - m); hidden keys hold -inf and get weight exactly 0
-        const f32x2 nm2 = pack2(-m, -m);
-        f32x2 sum2 = pack2(0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const f32x2 x =
-              fma2(pack2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), sc2, nm2);
-          const float e0 = ex2(lo2(x)), e1 = ex2(hi2(x));
-          sum2 = add2(sum2, pack2(e0, e1));
-          s[c] = pack_bf16x2(e0, e1);
-        }
-        l2 = add2(l2, sum2);
-        tmem_st32x32b_x64_lo(s_col, s);
-        // keys past the end of the sequence in its last tile: zero their V rows
-        // so that 0 * (stale data) cannot put a NaN into O (head a's 128 threads;
-        // thread t clears row t)
-        const bool last = kt == it.n - 1;
-        if (hh == 0 && last && kt * kN + kN > it.Lk) {
-          if (!(ok = warp_wait(bar(kBVFull + rv.idx), rv.ph))) { timeout = true; break; }
-          if (kt * kN + tid >= it.Lk) {
-            const uint4 zero = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int vh = 0; vh < 2; ++vh) {
-              const uint32_t vrow = sbase + kOffV + rv.idx * kTile + vh * kHalf + tid * 128;
-#pragma unroll
-              for (int cc = 0; cc < 8; ++cc) sts128(vrow + cc * 16, zero);
-            }
-          }
-          fence_proxy_async_smem();
-        }
-        tmem_wait_st();
-        if (last) {
-          // lse, and 1 / l for the output warps once they have read the previous item's
-          if (gi > 0 && !(ok = warp_wait(bar(kBLFree + hh), (gi - 1) & 1))) {
-            timeout = true;
-            break;
-          }
-          const float l = lo2(l2) + hi2(l2);
-          inv_l[hh * kM + row] = 1.f / l;
-          if (p.lse && row < it.rows)
-            p.lse[static_cast<int64_t>(it.q_begin + it.q0 + row) * p.Hq + it.h + hh] =
-                (m + __log2f(l)) * kLn2;
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bar(kBPFull + hh));
-          if (last) mbar_arrive(bar(kBLFull + hh));
-        }
-      }
-      if (!ok) break;
-      ++gi;
-      it = nx;
-      k = k2;
-      have = have_next;
-    }
-    if (timeout && lane == 0) record_error(p.err, kErrTimeout);
-    if (!ok && lane == 0) flags[0] = 1;
-    finish();
-    return;
-  }
-  if (warp < kQKWarp) {
-    // ------------------------------------------------------------ output
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(hp::kRegsOut));
-    // Warp 8 + qd: rows 32 qd + t of O_a, then of O_b (thread t holds its row,
-    // the 32x32b shape), 32 columns at a time, normalised and written as bf16;
-    // the accumulator is handed back once the last columns are in registers.
-    const int row = (warp & 3) * 32 + lane;
-    const uint32_t lb = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    bool ok = true, timeout = false;
-    int gi = 0;
-    int k = 0;
-    Item it;
-    bool have = next_item<kCausal, 2>(p, n_rounds, k, it, false);
-    while (have && ok) {
-      int k2 = k + 1;
-      Item nx;
-      const bool have_next = next_item<kCausal, 2>(p, n_rounds, k2, nx, false);
-      for (int hh = 0; hh < 2 && ok; ++hh) {
-        if (!(ok = warp_wait(bar(kBLFull + hh), gi & 1))) { timeout = true; break; }
-        const float il = inv_l[hh * kM + row];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBLFree + hh));
-        if (!(ok = warp_wait(bar(kBOFull + hh), gi & 1))) { timeout = true; break; }
-        tc_fence_after();
-        uint4* dst = reinterpret_cast<uint4*>(
-            p.out + (static_cast<int64_t>(it.q_begin + it.q0 + row) * p.Hq + it.h + hh) * kHeadDim);
-        const bool valid = row < it.rows;
-#pragma unroll 1
-        for (int c = 0; c < kHeadDim; c += 32) {
-          uint32_t o[32];
-          tmem_ld32x32b_x32_wait(lb + kColO + hh * kHeadDim + c, o);
-          uint4 w[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            w[j] = make_uint4(
-                pack_bf16x2(__uint_as_float(o[8 * j]) * il, __uint_as_float(o[8 * j + 1]) * il),
-                pack_bf16x2(__uint_as_float(o[8 * j + 2]) * il, __uint_as_float(o[8 * j + 3]) * il),
-                pack_bf16x2(__uint_as_float(o[8 * j + 4]) * il, __uint_as_float(o[8 * j + 5]) * il),
-                pack_bf16x2(__uint_as_float(o[8 * j + 6]) * il, __uint_as_float(o[8 * j + 7]) * il));
-          if (c == kHeadDim - 32) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kBOFree + hh));
-          }
-          if (valid) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) dst[c / 8 + j] = w[j];
-          }
-        }
-      }
-      if (!ok) break;
-      ++gi;
-      it = nx;
-      k = k2;
-      have = have_next;
-    }
-    if (timeout && lane == 0) record_error(p.err, kErrTimeout);
-    if (!ok && lane == 0) flags[0] = 1;
-    finish();
-    return;
-  }
-  // warps 12-15: one register share for the whole warpgroup, set at one place
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(hp::kRegsRest));
-  if (warp == kQKWarp) {
-    // ------------------------------------------------------------ TMA: Q and K
-    bool ok = true, stopped = false;
-    int gi = 0, gk = 0;
-    BlockIds ids;
-    Ring<kKStages> rk;
-    const int withhold = withheld_tile();   // test hook: K tiles from here on are never copied
-    // Q of head h0 + hh into its buffer once the previous item's S of that
-    // head is done with it; a sequence's ragged last tile is gathered with
-    // zero-filling copies.
-    auto load_q = [&](const Item& it, int qi, int hh) -> bool {
-      const uint32_t qdst = sbase + kOffQ + hh * kTile;
-      if (qi >= 1 && !warp_wait(bar(kBQEmpty + hh), (qi - 1) & 1)) return false;
-      if (it.rows < kM) {
-        const __nv_bfloat16* base =
-            p.q + (static_cast<int64_t>(it.q_begin + it.q0) * p.Hq + it.h + hh) * kHeadDim;
-        for (int e = lane; e < kM * 16; e += 32) {
-          const int r = e >> 4, piece = e & 15;
-          const bool valid = r < it.rows;
-          const __nv_bfloat16* src =
-              base + (valid ? static_cast<int64_t>(r) * p.Hq * kHeadDim + piece * 8 : 0);
-          cp_async16(qdst + (piece >> 3) * kHalf + r * 128 + (((piece & 7) ^ (r & 7)) << 4), src,
-                     valid ? 16u : 0u);
-        }
-        cp_async_wait_all();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBQFull + hh));
-      } else {
-        if (lane == 0) mbar_arrive_expect_tx(bar(kBQFull + hh), kTile);
-        __syncwarp();
-        const int ql = 2 * kKStages + 2 * hh;   // lanes of their own
-        if (lane == ql || lane == ql + 1)
-          tma_load_3d(qdst + (lane & 1) * kHalf, &qmap, bar(kBQFull + hh), (lane & 1) * 64,
-                      it.h + hh, it.q_begin + it.q0);
-      }
-      if (lane == 0) flags[3 + hh] = qi + 1;
-      __syncwarp();
-      return true;
-    };
-    int k = 0;
-    Item it;
-    bool have = next_item<kCausal, 2>(p, n_rounds, k, it, false);
-    while (have && ok) {
-      int k2 = k + 1;
-      Item nx;
-      const bool have_next = next_item<kCausal, 2>(p, n_rounds, k2, nx, false);
-      ids.chunk = -1;
-      for (int kt = 0; kt < it.n; ++kt, ++gk, rk.next()) {
-        if (__any_sync(kFull, flags[0] != 0)) { ok = false; break; }
-        if (gk >= withhold) { stopped = true; break; }
-        const int id = ids.get(it.table, p.maxblk, kt >> 1, lane, p.num_blocks, p.err);
-        const int slot = id * kBlockSize + (kt & 1) * kN;
-        if (gk >= kKStages && !warp_wait(bar(kBKEmpty + rk.idx), rk.ph ^ 1u)) {
-          ok = false;
-          if (lane == 0) record_error(p.err, kErrTimeout);
-          break;
-        }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar(kBKFull + rk.idx), kTile);
-          flags[1] = gk + 1;
-        }
-        __syncwarp();
-        if ((lane >> 1) == rk.idx)
-          tma_load_3d(sbase + kOffK + rk.idx * kTile + (lane & 1) * kHalf, &kmap,
-                      bar(kBKFull + rk.idx), (lane & 1) * 64, it.kvh, slot);
-        __syncwarp();
-        if (kt == 0 && (!load_q(it, gi, 0) || !load_q(it, gi, 1))) {
-          ok = false;
-          if (lane == 0) record_error(p.err, kErrTimeout);
-          break;
-        }
-      }
-      if (!ok || stopped) break;
-      ++gi;
-      it = nx;
-      k = k2;
-      have = have_next;
-    }
-    if (!ok && lane == 0) flags[0] = 1;
-  } else if (warp == kVWarp) {
-    // ------------------------------------------------------------ TMA: V
-    bool ok = true;
-    int gk = 0;
-    BlockIds ids;
-    Ring<kVStages> rv;
-    int k = 0;
-    Item it;
-    bool have = next_item<kCausal, 2>(p, n_rounds, k, it, false);
-    while (have && ok) {
-      int k2 = k + 1;
-      Item nx;
-      const bool have_next = next_item<kCausal, 2>(p, n_rounds, k2, nx, false);
-      ids.chunk = -1;
-      for (int kt = 0; kt < it.n; ++kt, ++gk, rv.next()) {
-        if (__any_sync(kFull, flags[0] != 0)) { ok = false; break; }
-        const int id = ids.get(it.table, p.maxblk, kt >> 1, lane, p.num_blocks, p.err);
-        const int slot = id * kBlockSize + (kt & 1) * kN;
-        if (gk >= kVStages && !warp_wait(bar(kBVEmpty + rv.idx), rv.ph ^ 1u)) {
-          ok = false;
-          if (lane == 0) record_error(p.err, kErrTimeout);
-          break;
-        }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar(kBVFull + rv.idx), kTile);
-          flags[2] = gk + 1;
-        }
-        __syncwarp();
-        if ((lane >> 1) == rv.idx)
-          tma_load_3d(sbase + kOffV + rv.idx * kTile + (lane & 1) * kHalf, &vmap,
-                      bar(kBVFull + rv.idx), (lane & 1) * 64, it.kvh, slot);
-        __syncwarp();
-      }
-      it = nx;
-      k = k2;
-      have = have_next;
-    }
-    if (!ok && lane == 0) flags[0] = 1;
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issue
-    // The whole warp runs the issue loop and waits; one elected lane issues
-    // each product and commit.
-    constexpr uint32_t idesc_s = idesc_bf16_f32(kM, kN, 0);        // B = K, K-major
-    constexpr uint32_t idesc_o = idesc_bf16_f32(kM, kHeadDim, 1);  // B = V, MN-major
-    bool ok = true, timeout = false;
-    int gi = 0, gk = 0;
-    Ring<kKStages> rk;
-    Ring<kVStages> rv;
-    // the PV of head b still to issue: tile gk - 1, its V stage and item
-    bool pend_b = false, pb_first = false, pb_last = false;
-    int pb_v = 0, pb_gi = 0;
-    // S of head hh from the K tile in stage ks_idx
-    auto issue_s = [&](int hh, int ks_idx) {
-      const uint32_t q_s = sbase + kOffQ + hh * kTile;
-      const uint32_t k_s = sbase + kOffK + ks_idx * kTile;
-      const uint32_t d = tmem + kColS + hh * kN;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
-        umma_bf16_warp(d, smem_desc_sw128(q_s + off, 16, 1024),
-                       smem_desc_sw128(k_s + off, 16, 1024), idesc_s, ks > 0);
-      }
-    };
-    // O_hh (+)= P_hh V: A = P from the first 64 columns of the head's S
-    auto issue_pv = [&](int hh, int v_idx, bool accumulate) {
-      const uint32_t v_s = sbase + kOffV + v_idx * kTile;
-      const uint32_t p_t = tmem + kColS + hh * kN;
-      const uint32_t d = tmem + kColO + hh * kHeadDim;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        umma_bf16_tmem_a_warp(d, p_t + ks * 8, smem_desc_sw128(v_s + ks * 2048, kHalf, 1024),
-                              idesc_o, (accumulate || ks > 0) ? 1u : 0u);
-    };
-    // PV of head b for tile gk - 1 (its V stage was waited for by PV_a)
-    auto flush_b = [&]() -> bool {
-      if (!warp_wait(bar(kBPFull + 1), (gk - 1) & 1)) return false;
-      if (pb_first && pb_gi > 0 && !warp_wait(bar(kBOFree + 1), (pb_gi - 1) & 1)) return false;
-      tc_fence_after();
-      issue_pv(1, pb_v, !pb_first);
-      umma_commit_warp(bar(kBPVDone + 1));
-      umma_commit_warp(bar(kBVEmpty + pb_v));
-      if (pb_last) umma_commit_warp(bar(kBOFull + 1));
-      pend_b = false;
-      return true;
-    };
-    int k = 0;
-    Item it;
-    bool have = next_item<kCausal, 2>(p, n_rounds, k, it, false);
-    while (have && ok) {
-      int k2 = k + 1;
-      Item nx;
-      const bool have_next = next_item<kCausal, 2>(p, n_rounds, k2, nx, false);
-      for (int kt = 0; kt < it.n; ++kt, ++gk, rk.next(), rv.next()) {
-        if (__any_sync(kFull, flags[0] != 0)) { ok = false; break; }
-        if (!warp_wait(bar(kBKFull + rk.idx), rk.ph) ||
-            (kt == 0 && !warp_wait(bar(kBQFull + 0), gi & 1))) {
-          ok = false;
-          timeout = true;
-          break;
-        }
-        tc_fence_after();
-        // S_a(gk), once PV_a(gk - 1) has read P_a from the same columns
-        if (gk > 0 && !warp_wait(bar(kBPVDone + 0), (gk - 1) & 1)) {
-          ok = false;
-          timeout = true;
-          break;
-        }
-        tc_fence_after();
-        issue_s(0, rk.idx);
-        umma_commit_warp(bar(kBSFull + 0));
-        if (kt == it.n - 1) umma_commit_warp(bar(kBQEmpty + 0));
-        // PV_b(gk - 1)
-        if (pend_b && !flush_b()) {
-          ok = false;
-          timeout = true;
-          break;
-        }
-        // S_b(gk)
-        if (kt == 0 && !warp_wait(bar(kBQFull + 1), gi & 1)) {
-          ok = false;
-          timeout = true;
-          break;
-        }
-        if (gk > 0 && !warp_wait(bar(kBPVDone + 1), (gk - 1) & 1)) {
-          ok = false;
-          timeout = true;
-          break;
-        }
-        tc_fence_after();
-        issue_s(1, rk.idx);
-        umma_commit_warp(bar(kBSFull + 1));
-        umma_commit_warp(bar(kBKEmpty + rk.idx));
-        if (kt == it.n - 1) umma_commit_warp(bar(kBQEmpty + 1));
-        // PV_a(gk)
-        if (!warp_wait(bar(kBVFull + rv.idx), rv.ph) || !warp_wait(bar(kBPFull + 0), gk & 1) ||
-            (kt == 0 && gi > 0 && !warp_wait(bar(kBOFree + 0), (gi - 1) & 1))) {
-          ok = false;
-          timeout = true;
-          break;
-        }
-        tc_fence_after();
-        issue_pv(0, rv.idx, kt > 0);
-        umma_commit_warp(bar(kBPVDone + 0));
-        if (kt == it.n - 1) umma_commit_warp(bar(kBOFull + 0));
-        pend_b = true;
-        pb_first = kt == 0;
-        pb_last = kt == it.n - 1;
-        pb_v = rv.idx;
-        pb_gi = gi;
-      }
-      if (!ok) break;
-      ++gi;
-      it = nx;
-      k = k2;
-      have = have_next;
-    }
-    if (ok && pend_b && !flush_b()) {
-      ok = false;
-      timeout = true;
-    }
-    if (timeout && lane == 0) record_error(p.err, kErrTimeout);
-    if (!ok && lane == 0) flags[0] = 1;
-    // every MMA this warp issued has completed once this arrives
-    umma_commit_warp(bar(kBDrain));
-    (void)warp_wait(bar(kBDrain), 0);
-  }
-  finish();
-}
-
 template <int kMode>
 bool set_smem_attr() {
   static bool attr_set[64] = {};
@@ -1464,27 +840,6 @@ bool set_smem_attr() {
     if (cudaFuncSetAttribute(paged_prefill_kernel<kMode>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes) != cudaSuccess)
-      return false;
-    attr_set[dev] = true;
-  }
-  return true;
-}
-
-// The head-pair kernel moves registers between its warpgroups; it is only
-// launched when the build gave it exactly the 128 registers per thread that
-// the shares were added up against (otherwise the larger shares could never be
-// granted).
-bool set_pair_smem_attr() {
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, paged_prefill_pair_kernel) != cudaSuccess ||
-        fa.numRegs != hp::kRegsLaunch)
-      return false;
-    if (cudaFuncSetAttribute(paged_prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             hp::kSmemBytes) != cudaSuccess)
       return false;
     attr_set[dev] = true;
   }
@@ -1536,16 +891,6 @@ int launch_prefill(const PrefillArgs& a, unsigned* err, cudaStream_t stream) {
   prm.n_qt = (a.max_seqlen_q + kM - 1) / kM;
   prm.num_blocks = a.num_blocks;
   prm.scale_log2 = a.scale * 1.4426950408889634f;
-  if ((a.Hq / a.Hkv) % 2 == 0) {
-    // two query heads of one kv head per item
-    const int64_t items = static_cast<int64_t>(prm.n_qt) * a.B * (a.Hq / 2);
-    if (items > INT32_MAX) return PKV_ERR_SHAPE;
-    prm.n_items = static_cast<int>(items);
-    if (!set_pair_smem_attr()) return PKV_ERR_LAUNCH;
-    paged_prefill_pair_kernel<<<grid_for(prm.n_items), hp::kThreads, hp::kSmemBytes, stream>>>(
-        qm, km, vm, prm);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
-  }
   const int64_t items = static_cast<int64_t>(prm.n_qt) * a.B * a.Hq;
   if (items > INT32_MAX) return PKV_ERR_SHAPE;
   prm.n_items = static_cast<int>(items);
