@@ -550,8 +550,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   // the ring up front and refilling each stage as soon as every consumer warp
   // has released it.  Otherwise the consumer warps copy: bf16: warp w loads
   // the w-th of those four boxes; E4M3: warps 0 and 1 the K and the V box.
-  // Lane 0 of each issuing warp fills its part of the ring up front and
-  // refills the stage released one tile earlier.
+  // Each issuing warp fills its part of the ring up front and refills the
+  // stage released one tile earlier.  The whole warp runs the issue code and
+  // waits; one elected lane issues each copy (issuing from a lane-0 branch
+  // spent about 440 cycles per tile there).
   const uint64_t policy = l2_policy_evict_first();
   const int withhold = withheld_tile();   // test hook: tiles from here on are never copied
   auto issue = [&](int it) {
@@ -560,37 +562,40 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     const int tok = tok_begin + it * kTile;
     const int slot = sblk[tok / kBlockSize - blk_begin] * kBlockSize + tok % kBlockSize;
     // the tile holding the new token is read only once that token is written
-    if (store_here && it == n_tiles - 1 && !mbar_wait(stored_bar, 0)) {
-      record_error(p.err, kErrTimeout);
-      flags[0] = 1;
+    if (store_here && it == n_tiles - 1 && !__all_sync(0xffffffffu, mbar_wait(stored_bar, 0))) {
+      if (lane == 0) {
+        record_error(p.err, kErrTimeout);
+        flags[0] = 1;
+      }
       return;
     }
     if constexpr (kProd) {
       const uint32_t dst = smem_addr(smem + s * kStageB);
-      mbar_arrive_expect_tx(full_bar(s), kStageB);
-      tma_load_3d_hint(dst, &kmap, full_bar(s), 0, kvh0, slot, policy);
+      mbar_arrive_expect_tx_warp(full_bar(s), kStageB);
+      tma_load_3d_hint_warp(dst, &kmap, full_bar(s), 0, kvh0, slot, policy);
       if constexpr (!kFp8)
-        tma_load_3d_hint(dst + kHalfBytes, &kmap, full_bar(s), 64, kvh0, slot, policy);
-      tma_load_3d_hint(dst + kOpBytes, &vmap, full_bar(s), 0, kvh0, slot, policy);
+        tma_load_3d_hint_warp(dst + kHalfBytes, &kmap, full_bar(s), 64, kvh0, slot, policy);
+      tma_load_3d_hint_warp(dst + kOpBytes, &vmap, full_bar(s), 0, kvh0, slot, policy);
       if constexpr (!kFp8)
-        tma_load_3d_hint(dst + kOpBytes + kHalfBytes, &vmap, full_bar(s), 64, kvh0, slot, policy);
+        tma_load_3d_hint_warp(dst + kOpBytes + kHalfBytes, &vmap, full_bar(s), 64, kvh0, slot,
+                              policy);
     } else if constexpr (kFp8) {
       // warp 0: the K tile, warp 1: the V tile (one 128-byte-wide box each)
       const uint32_t dst = smem_addr(smem + s * kStageB) + warp * kOpBytes;
-      mbar_arrive_expect_tx(full_bar(s), kOpBytes);
+      mbar_arrive_expect_tx_warp(full_bar(s), kOpBytes);
       if (warp == 0)
-        tma_load_3d_hint(dst, &kmap, full_bar(s), 0, kvh0, slot, policy);
+        tma_load_3d_hint_warp(dst, &kmap, full_bar(s), 0, kvh0, slot, policy);
       else
-        tma_load_3d_hint(dst, &vmap, full_bar(s), 0, kvh0, slot, policy);
+        tma_load_3d_hint_warp(dst, &vmap, full_bar(s), 0, kvh0, slot, policy);
     } else {
       const uint32_t dst = smem_addr(smem + s * kStageB) + warp * kHalfBytes;
-      mbar_arrive_expect_tx(full_bar(s), kHalfBytes);
+      mbar_arrive_expect_tx_warp(full_bar(s), kHalfBytes);
       if (warp < 2)
-        tma_load_3d_hint(dst, &kmap, full_bar(s), (warp & 1) * 64, kvh0, slot, policy);
+        tma_load_3d_hint_warp(dst, &kmap, full_bar(s), (warp & 1) * 64, kvh0, slot, policy);
       else
-        tma_load_3d_hint(dst, &vmap, full_bar(s), (warp & 1) * 64, kvh0, slot, policy);
+        tma_load_3d_hint_warp(dst, &vmap, full_bar(s), (warp & 1) * 64, kvh0, slot, policy);
     }
-    atomicMax(const_cast<int*>(flags + 2), it + 1);
+    if (lane == 0) atomicMax(const_cast<int*>(flags + 2), it + 1);
   };
   if (warp == 0) {
     if (lane == 0) {
@@ -629,7 +634,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     if (lane == 0) mbar_arrive(stored_bar);
   }
   const bool prodw = kProd && warp == kConsumerWarps;  // the producer warp
-  if (lane == 0 && (kProd ? prodw : warp < kIssuers))
+  if (kProd ? prodw : warp < kIssuers)
     for (int it = 0; it < kStagesN && it < n_tiles; ++it) issue(it);
 
   {
@@ -661,16 +666,17 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     float m_run = -INFINITY;  // log2-domain running max of row gq
     float l_run = 0.f;        // sum of the weights of this lane's tokens
     if (prodw) {
-      if (lane == 0) {
-        for (int it = kStagesN; it < n_tiles && !flags[0]; ++it) {
-          const int pv = it - kStagesN;
-          if (!mbar_wait(empty_bar(pv % kStagesN), (pv / kStagesN) & 1)) {
+      for (int it = kStagesN; it < n_tiles; ++it) {
+        if (__any_sync(0xffffffffu, flags[0] != 0)) break;
+        const int pv = it - kStagesN;
+        if (!__all_sync(0xffffffffu, mbar_wait(empty_bar(pv % kStagesN), (pv / kStagesN) & 1))) {
+          if (lane == 0) {
             record_error(p.err, kErrTimeout);
             flags[0] = 1;
-            break;
           }
-          issue(it);
+          break;
         }
+        issue(it);
       }
       __syncwarp();
     } else {
@@ -711,18 +717,17 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       consume_stage<G, kMQ, kFp8>(kb, kb + kOpBytes, warp, gq, c, qa, qmul, n_valid,
                                   lim - it * kTile, o, m_run, l_run);
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(empty_bar(s));
-        // refill the stage released one tile ago: by now every warp has
-        // usually released it too, so the issuing lanes seldom wait
-        const int pv = it - 1;
-        if (!kProd && warp < kIssuers && pv >= 0 && pv + kStagesN < n_tiles && !flags[0]) {
-          if (mbar_wait(empty_bar(pv % kStagesN), (pv / kStagesN) & 1)) {
-            issue(pv + kStagesN);
-          } else {
-            record_error(p.err, kErrTimeout);
-            flags[0] = 1;
-          }
+      if (lane == 0) mbar_arrive(empty_bar(s));
+      // refill the stage released one tile ago: by now every warp has usually
+      // released it too, so the issuing warps seldom wait
+      const int pv = it - 1;
+      if (!kProd && warp < kIssuers && pv >= 0 && pv + kStagesN < n_tiles &&
+          !__any_sync(0xffffffffu, flags[0] != 0)) {
+        if (__all_sync(0xffffffffu, mbar_wait(empty_bar(pv % kStagesN), (pv / kStagesN) & 1))) {
+          issue(pv + kStagesN);
+        } else if (lane == 0) {
+          record_error(p.err, kErrTimeout);
+          flags[0] = 1;
         }
       }
       __syncwarp();
