@@ -461,6 +461,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   auto empty_bar = [&](int s) { return bars + 8u * (kStagesN + s); };
   const uint32_t stored_bar = bars + 8u * (2 * kStagesN);  // fused store: the new row written
 
+  // Programmatic dependent launch: the next kernel of the stream may be
+  // scheduled once every block of this one has started, and this kernel
+  // reads no global memory before the grids it depends on have completed.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int split = blockIdx.x;
   const int hg = blockIdx.y;  // kv head * head_groups + query head group
   const int b = blockIdx.z;
@@ -841,9 +846,22 @@ int launch_g(const DecodeArgs& a, const DecodePlan& plan, const DecodeParams& pr
       return PKV_ERR_LAUNCH;
     attr_set[dev] = true;
   }
-  dim3 grid(plan.num_splits, a.Hkv * plan.head_groups, a.B);
-  paged_decode_kernel<G, kMQ, kFp8, kProd>
-      <<<grid, kProd ? kThreads + 32 : kThreads, L::kBytes, stream>>>(km, vm, prm);
+  // launched with programmatic stream serialization: it may start while the
+  // previous kernel of the stream finishes, and waits (griddepcontrol.wait)
+  // before its first global read
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan.num_splits, a.Hkv * plan.head_groups, a.B);
+  cfg.blockDim = dim3(kProd ? kThreads + 32 : kThreads);
+  cfg.dynamicSmemBytes = L::kBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, paged_decode_kernel<G, kMQ, kFp8, kProd>, km, vm, prm) !=
+      cudaSuccess)
+    return PKV_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
 }
 
