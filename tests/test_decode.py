@@ -71,12 +71,26 @@ def test_ragged_tile_tails():
 @pytest.mark.parametrize("Hq,Hkv", [(8, 2), (16, 4), (32, 4)])
 def test_small_batch_tile_splits(Hq, Hkv):
     """Batches too small to fill the GPU with one-block splits split into
-    64-token tiles (ranges that start inside a block); every tile and block
-    residue of the context length."""
-    lens = [1, 63, 64, 65, 200, 256, 257, 700]
-    w = W.make_decode(lens, Hq, Hkv, 24, 3050 + Hq)
-    assert pkv.paged_decode_num_splits(w.B, Hq, Hkv, 128, w.block_tables.shape[1]) == 12
+    64-token tiles (ranges that start inside a block) once a context spans four
+    blocks or more; every tile and block residue of the context length."""
+    lens = [1, 63, 64, 65, 200, 256, 257, 700, 1000]
+    w = W.make_decode(lens, Hq, Hkv, 32, 3050 + Hq)
+    maxblk = w.block_tables.shape[1]
+    assert maxblk == 4
+    assert pkv.paged_decode_num_splits(w.B, Hq, Hkv, 128, maxblk) == 4 * maxblk
     run_and_check(w, what=f"tile splits Hq={Hq},Hkv={Hkv}")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (16, 4), (32, 4)])
+def test_small_batch_short_contexts_one_split(Hq, Hkv):
+    """A small batch whose contexts span at most three blocks runs one split per
+    sequence (no partials, no merge, no workspace)."""
+    lens = [1, 63, 64, 65, 200, 256, 257, 700]
+    w = W.make_decode(lens, Hq, Hkv, 24, 3070 + Hq)
+    maxblk = w.block_tables.shape[1]
+    assert maxblk == 3
+    assert pkv.paged_decode_num_splits(w.B, Hq, Hkv, 128, maxblk) == 1
+    run_and_check(w, what=f"one split Hq={Hq},Hkv={Hkv}")
 
 
 def test_empty_context_gives_zero_and_neg_inf():

@@ -61,10 +61,10 @@ def test_decode_wait_runs_out_then_recovers(wait_fault, num_splits):
 
 
 def test_small_batch_decode_wait_runs_out_then_recovers(wait_fault):
-    # a batch too small to fill the GPU: 64-token tile splits, one or two tiles
-    # per block, the 2-stage consumer-issued form; every block's first tile is
-    # withheld
-    w = W.make_decode([300, 513, 40], 16, 8, 8, 8120, store_new_token=False)
+    # a batch too small to fill the GPU, one context of four blocks: 64-token
+    # tile splits, the 2-stage consumer-issued form; every block's first tile
+    # is withheld
+    w = W.make_decode([300, 900, 40], 16, 8, 8, 8120, store_new_token=False)
     dev = "cuda"
     maxblk = w.block_tables.shape[1]
     assert pkv.paged_decode_num_splits(w.B, w.Hq, w.Hkv, w.D, maxblk, w.block_size, 0) > maxblk
