@@ -20,7 +20,8 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libpkv.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
-SOURCES = ["api.cu", "store.cu", "decode.cu", "prefill.cu", "noalloc.cu", "blocks.cpp"]
+SOURCES = ["api.cu", "store.cu", "decode.cu", "prefill.cu", "noalloc.cu", "graphs.cu",
+           "blocks.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
               "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]

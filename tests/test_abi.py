@@ -1,4 +1,4 @@
-"""The C-ABI library loads and exports every symbol include/pkv.h declares; host
+"""The C-ABI library loads and exports every symbol include/*.h declares; host
 argument checks answer without touching a GPU (no GPU needed)."""
 import ctypes
 import os
@@ -10,12 +10,14 @@ from paged_kv_cache_214_gb300 import build as B
 from paged_kv_cache_214_gb300 import pkv
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "pkv.h")
+HEADERS = ("pkv.h", "pkv_blocks.h", "pkv_graphs.h")
 
 
-def declared_functions():
-    text = open(HEADER).read()
+def declared_functions(header=HEADER):
+    text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return re.findall(r"^\s*(?:int|size_t|const char\s*\*)\s*(\w+)\s*\(", text, flags=re.M)
+    return re.findall(r"^\s*(?:int|int64_t|size_t|void|const char\s*\*|pkv_block_manager\s*\*)"
+                      r"\s*(\w+)\s*\(", text, flags=re.M)
 
 
 @pytest.fixture(scope="module")
@@ -32,9 +34,12 @@ def test_header_declares_the_hot_path():
 
 
 def test_every_declared_symbol_is_exported(lib):
-    for name in declared_functions():
-        assert hasattr(lib, name), name
-        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+    for header in HEADERS:
+        names = declared_functions(os.path.join(os.path.dirname(HEADER), header))
+        assert names, header
+        for name in names:
+            assert hasattr(lib, name), name
+            assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
 
 
 def test_host_argument_checks(lib):
@@ -171,10 +176,11 @@ def test_bindings_declare_every_signature(lib):
     """ctypes passes undeclared integer arguments as 32-bit ints, which would
     truncate 64-bit device pointers: every exported function must carry
     argtypes / restype from the bindings."""
-    from paged_kv_cache_214_gb300 import blocks
+    from paged_kv_cache_214_gb300 import blocks, graphs
     blocks._lib()
+    graphs._lib()
     hdr_dir = os.path.dirname(HEADER)
-    for header in ("pkv.h", "pkv_blocks.h"):
+    for header in HEADERS:
         text = re.sub(r"/\*.*?\*/", "", open(os.path.join(hdr_dir, header)).read(), flags=re.S)
         names = re.findall(r"^\s*(?:int|int64_t|size_t|void|const char\s*\*|pkv_block_manager\s*\*)"
                            r"\s*(\w+)\s*\(", text, flags=re.M)
