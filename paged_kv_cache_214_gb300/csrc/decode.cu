@@ -165,10 +165,15 @@ __device__ __forceinline__ void merge_row(const float* lrow, const float* orow, 
 // with one (kProd), 6 stages at two blocks per SM (the fifth warp's registers
 // leave no room for a third block).  bf16 without a producer warp (batches
 // split into 64-token tiles, one or a few per block): 2 stages, three blocks
-// per SM, so that all of such a batch's blocks are resident at once.
-template <bool kFp8, bool kProd = false>
+// per SM, so that all of such a batch's blocks are resident at once.  bf16
+// with two consumer groups (kGroups = 2: one block per SM, batches whose
+// one-split grid fits one wave): 6 stages; an even count keeps each stage's
+// tiles in one group (see the consumer notes in the kernel).
+template <bool kFp8, bool kProd = false, int kGroups = 1>
 struct Geo {
-  static constexpr int kStagesN = kFp8 ? (kProd ? 6 : 4) : (kProd ? 3 : 2);
+  static_assert(kGroups == 1 || (kGroups == 2 && kProd && !kFp8), "two groups: bf16, producer warp");
+  static constexpr int kStagesN = kGroups == 2 ? 6 : kFp8 ? (kProd ? 6 : 4) : (kProd ? 3 : 2);
+  static_assert(kGroups == 1 || kStagesN % 2 == 0, "two groups need an even stage count");
   static constexpr int kOpBytes = kTile * (kFp8 ? 128 : 256);  // one of K or V for a stage
   static constexpr int kStageB = 2 * kOpBytes;
   static constexpr int kIssuers = kFp8 ? 2 : 4;
@@ -176,17 +181,18 @@ struct Geo {
 static_assert(Geo<false, true>::kStagesN == kStages && Geo<false, true>::kStageB == kStageBytes,
               "geometry");
 
-template <int G, bool kFp8 = false, bool kProd = false>
+template <int G, bool kFp8 = false, bool kProd = false, int kGroups = 1>
 struct SmemLayout {
-  static constexpr int kStages = Geo<kFp8, kProd>::kStagesN;
-  static constexpr int kStageBytes = Geo<kFp8, kProd>::kStageB;
-  // [4][G][128] f32, over the stage ring: written only once every warp is
+  static constexpr int kStages = Geo<kFp8, kProd, kGroups>::kStagesN;
+  static constexpr int kStageBytes = Geo<kFp8, kProd, kGroups>::kStageB;
+  static constexpr int kCW = kConsumerWarps * kGroups;   // consumer warps
+  // [kCW][G][128] f32, over the stage ring: written only once every warp is
   // done with the stages and no copy is in flight
   static constexpr int kMergeO = 0;
-  static_assert(kConsumerWarps * G * 128 * 4 <= kStages * kStageBytes, "merge buffer");
-  static constexpr int kMergeM = kStages * kStageBytes;                      // [4][G]
-  static constexpr int kMergeL = kMergeM + kConsumerWarps * G * 4;           // [4][G]
-  static constexpr int kBlk = kMergeL + kConsumerWarps * G * 4;              // [32] int
+  static_assert(kCW * G * 128 * 4 <= kStages * kStageBytes, "merge buffer");
+  static constexpr int kMergeM = kStages * kStageBytes;                      // [kCW][G]
+  static constexpr int kMergeL = kMergeM + kCW * G * 4;                      // [kCW][G]
+  static constexpr int kBlk = kMergeL + kCW * G * 4;                         // [32] int
   static constexpr int kBars = kBlk + kMaxSplitBlocks * 4;                   // full[], empty[]
   static constexpr int kFlags = kBars + (2 * kStages + 1) * 8;  // + stored; abort, last, issued
   static constexpr int kEnd = kFlags + 16;
@@ -439,15 +445,17 @@ __device__ __forceinline__ void store_new_row(const DecodeParams& p, int b, int 
 // warp issues every copy, so that no consumer warp waits for the others to
 // release a stage before its next tile.  One kv head per block; G of its
 // query heads.
-template <int G, bool kMQ, bool kFp8, bool kProd>
-__global__ void __launch_bounds__(kProd ? kThreads + 32 : kThreads, kProd ? 2 : 3)
+template <int G, bool kMQ, bool kFp8, bool kProd, int kGroups = 1>
+__global__ void __launch_bounds__(kProd ? kThreads * kGroups + 32 : kThreads,
+                                  kGroups == 2 ? 1 : (kProd ? 2 : 3))
 paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
-  using L = SmemLayout<G, kFp8, kProd>;
-  constexpr int kStagesN = Geo<kFp8, kProd>::kStagesN;
-  constexpr int kStageB = Geo<kFp8, kProd>::kStageB;
-  constexpr int kOpBytes = Geo<kFp8, kProd>::kOpBytes;
-  constexpr int kIssuers = Geo<kFp8, kProd>::kIssuers;
+  using L = SmemLayout<G, kFp8, kProd, kGroups>;
+  constexpr int kStagesN = Geo<kFp8, kProd, kGroups>::kStagesN;
+  constexpr int kStageB = Geo<kFp8, kProd, kGroups>::kStageB;
+  constexpr int kOpBytes = Geo<kFp8, kProd, kGroups>::kOpBytes;
+  constexpr int kIssuers = Geo<kFp8, kProd, kGroups>::kIssuers;
+  constexpr int kCW = L::kCW;   // consumer warps
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -638,7 +646,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     __syncwarp();
     if (lane == 0) mbar_arrive(stored_bar);
   }
-  const bool prodw = kProd && warp == kConsumerWarps;  // the producer warp
+  const bool prodw = kProd && warp == kCW;  // the producer warp
   if (kProd ? prodw : warp < kIssuers)
     for (int it = 0; it < kStagesN && it < n_tiles; ++it) issue(it);
 
@@ -709,7 +717,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
     // keys of this split row gq may see (several query positions only)
     const int lim = kMQ ? key_limit(qhead(gq < G ? gq : 0)) - tok_begin : 0;
 
-    for (int it = 0; it < n_tiles; ++it) {
+    // Two groups (kGroups = 2): warps [4 grp, 4 grp + 4) take tiles grp,
+    // grp + 2, ...; with an even stage count a stage only ever holds one
+    // group's tiles, so a warp that waits for tile it has itself consumed the
+    // stage's previous tile, it - kStagesN (the wait is never two phases
+    // ahead), and each tile's empty barrier counts that group's four warps.
+    const int grp = warp / kConsumerWarps;
+    const int wg = warp % kConsumerWarps;   // the warp's 16-token slice of a tile
+    for (int it = grp; it < n_tiles; it += kGroups) {
       const int s = it % kStagesN;
       if (flags[0]) break;
       if (!mbar_wait(full_bar(s), (it / kStagesN) & 1)) {
@@ -719,7 +734,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
       }
       const int n_valid = min(kTile, tok_end - (tok_begin + it * kTile));
       const uint32_t kb = smem_addr(smem + s * kStageB);
-      consume_stage<G, kMQ, kFp8>(kb, kb + kOpBytes, warp, gq, c, qa, qmul, n_valid,
+      consume_stage<G, kMQ, kFp8>(kb, kb + kOpBytes, wg, gq, c, qa, qmul, n_valid,
                                   lim - it * kTile, o, m_run, l_run);
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar(s));
@@ -770,7 +785,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   }
 
   __syncthreads();
-  if (prodw) return;
+  // the producer warp and a second consumer group leave: the epilogue (and
+  // its named barrier) runs on threads 0..127
+  if (tid >= kConsumerWarps * 32) return;
 
   // ---------------------------------------------------------------- epilogue
   // thread tid (0..127) owns dim d = tid of every head
@@ -779,10 +796,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   for (int h = 0; h < G; ++h) {
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge_m[w * G + h]);
+    for (int w = 0; w < kCW; ++w) M = fmaxf(M, merge_m[w * G + h]);
     float Ls = 0.f, Os = 0.f;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
+    for (int w = 0; w < kCW; ++w) {
       const float c = rescale(merge_m[w * G + h], M);
       Ls += merge_l[w * G + h] * c;
       Os += merge_o[(w * G + h) * kHeadDim + d] * c;
@@ -831,16 +848,17 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   if (tid == 0) *counter = 0u;  // ready for the next call
 }
 
-template <int G, bool kMQ, bool kFp8, bool kProd>
+template <int G, bool kMQ, bool kFp8, bool kProd, int kGroups = 1>
 int launch_g(const DecodeArgs& a, const DecodePlan& plan, const DecodeParams& prm,
              const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t stream) {
-  using L = SmemLayout<G, kFp8, kProd>;
-  static_assert(L::kBytes <= 113 * 1024, "two blocks per SM must fit");
+  using L = SmemLayout<G, kFp8, kProd, kGroups>;
+  static_assert(L::kBytes <= (kGroups == 2 ? 227 : 113) * 1024,
+                "two blocks per SM (one with two consumer groups) must fit");
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(paged_decode_kernel<G, kMQ, kFp8, kProd>,
+    if (cudaFuncSetAttribute(paged_decode_kernel<G, kMQ, kFp8, kProd, kGroups>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              L::kBytes) != cudaSuccess)
       return PKV_ERR_LAUNCH;
@@ -851,7 +869,7 @@ int launch_g(const DecodeArgs& a, const DecodePlan& plan, const DecodeParams& pr
   // before its first global read
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.num_splits, a.Hkv * plan.head_groups, a.B);
-  cfg.blockDim = dim3(kProd ? kThreads + 32 : kThreads);
+  cfg.blockDim = dim3(kProd ? kThreads * kGroups + 32 : kThreads);
   cfg.dynamicSmemBytes = L::kBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -859,7 +877,7 @@ int launch_g(const DecodeArgs& a, const DecodePlan& plan, const DecodeParams& pr
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, paged_decode_kernel<G, kMQ, kFp8, kProd>, km, vm, prm) !=
+  if (cudaLaunchKernelEx(&cfg, paged_decode_kernel<G, kMQ, kFp8, kProd, kGroups>, km, vm, prm) !=
       cudaSuccess)
     return PKV_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
@@ -884,6 +902,7 @@ int plan_decode(int B, int Hq, int Hkv, int max_blocks_per_seq, int num_splits,
   const int G = (g % 8 == 0) ? 8 : (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1;
   plan->heads_per_cta = G;
   plan->head_groups = g / G;
+  plan->consumer_groups = 1;
   // One kv head per block.  (Reading two kv heads per block as 512-byte
   // chunks per token measured 2% slower on GB300 on the batch-64 decode and
   // slower on short contexts.)
@@ -923,6 +942,10 @@ int plan_decode(int B, int Hq, int Hkv, int max_blocks_per_seq, int num_splits,
     // us with 64-token splits; 13.3 against 14.3 us per call).
     S = 1;
     plan->split_tokens = maxblk * kBlockSize;
+    // The grid (one block per sequence and kv head group) is under one wave,
+    // so each block may take a whole SM: two groups of consumer warps take
+    // alternate tiles, which halves the chain of tiles of the longest context.
+    plan->consumer_groups = 2;
   } else if (small) {
     constexpr int kTilesPerBlock = kBlockSize / kTile;
     const int64_t tiles = static_cast<int64_t>(maxblk) * kTilesPerBlock;
@@ -1058,6 +1081,16 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
       default:
         return prod ? launch_g<1, false, true, true>(a, plan, prm, km, vm, stream)
                     : launch_g<1, false, true, false>(a, plan, prm, km, vm, stream);
+    }
+  }
+  // bf16 single-token batches of one split per sequence under one wave: the
+  // producer-warp form with two consumer groups (one block per SM)
+  if (plan.consumer_groups == 2 && a.q_len == 1) {
+    switch (plan.heads_per_cta) {
+      case 8: return launch_g<8, false, false, true, 2>(a, plan, prm, km, vm, stream);
+      case 4: return launch_g<4, false, false, true, 2>(a, plan, prm, km, vm, stream);
+      case 2: return launch_g<2, false, false, true, 2>(a, plan, prm, km, vm, stream);
+      default: return launch_g<1, false, false, true, 2>(a, plan, prm, km, vm, stream);
     }
   }
   // bf16 batches split into 64-token tiles: the 2-stage consumer-issued form

@@ -92,6 +92,7 @@ struct DecodePlan {
   int head_groups;    // (Hq/Hkv) / G
   int split_tokens;   // tokens per split: whole blocks, or whole 64-token tiles
   int num_splits;     // S
+  int consumer_groups;  // 2: bf16 single-token decode with two consumer groups per block
   size_t prefix_offset;  // byte offset of the shared-prefix partials (if any)
   int prefix_splits;     // key ranges of the shared-prefix pass
   int prefix_kt_per;     // 128-key tiles per range

@@ -81,10 +81,12 @@ def test_small_batch_tile_splits(Hq, Hkv):
     run_and_check(w, what=f"tile splits Hq={Hq},Hkv={Hkv}")
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (16, 4), (32, 4)])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 4), (8, 2), (16, 4), (32, 4)])
 def test_small_batch_short_contexts_one_split(Hq, Hkv):
     """A small batch whose contexts span at most three blocks runs one split per
-    sequence (no partials, no merge, no workspace)."""
+    sequence (no partials, no merge, no workspace), on the form with two
+    consumer groups taking alternate tiles (1, 2, 4 and 8 query heads per
+    block)."""
     lens = [1, 63, 64, 65, 200, 256, 257, 700]
     w = W.make_decode(lens, Hq, Hkv, 24, 3070 + Hq)
     maxblk = w.block_tables.shape[1]

@@ -86,6 +86,33 @@ def test_small_batch_decode_wait_runs_out_then_recovers(wait_fault):
     assert_close(out, lse, ref_o, ref_l, "small-batch decode after a timeout")
 
 
+def test_one_split_two_group_decode_wait_runs_out_then_recovers(wait_fault):
+    # a small batch of contexts of at most three blocks: one split per
+    # sequence, two consumer groups taking alternate tiles; every block's first
+    # tile is withheld, so both groups' waits and the producer's run out
+    w = W.make_decode([300, 513, 40], 16, 8, 8, 8130, store_new_token=False)
+    dev = "cuda"
+    maxblk = w.block_tables.shape[1]
+    assert maxblk == 3
+    assert pkv.paged_decode_num_splits(w.B, w.Hq, w.Hkv, w.D, maxblk, w.block_size, 0) == 1
+    args = (w.q.to(dev), w.k_cache.to(dev), w.v_cache.to(dev), w.block_tables.to(dev),
+            w.context_lens.to(dev), w.scale)
+    assert pkv.get_device_error() == pkv.PKV_OK
+    wait_fault(0)
+    t0 = time.perf_counter()
+    pkv.paged_decode_attention(*args)
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 10.0
+    assert pkv.get_device_error() == pkv.PKV_ERR_TIMEOUT
+    pkv.testing_set_wait_fault(0, -1)
+    out, lse = pkv.paged_decode_attention(*args)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == pkv.PKV_OK
+    ref_o, ref_l = oracle.decode(bits(w.q), bits(w.k_cache), bits(w.v_cache),
+                                 w.block_tables.numpy(), w.context_lens.numpy(), w.scale)
+    assert_close(out, lse, ref_o, ref_l, "one-split decode after a timeout")
+
+
 @pytest.mark.parametrize("num_splits", [0, 2])
 def test_fp8_decode_wait_runs_out_then_recovers(wait_fault, num_splits):
     # E4M3 pools: the consumer-issued form (automatic splits of this batch) and
