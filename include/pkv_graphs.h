@@ -12,7 +12,8 @@
  *
  * A runner owns, for one pool and one set of shapes, one graph per bucket b of
  * the step "pad rows [B, b), then paged_decode_attention_store (or
- * paged_decode_attention_fp8_store) over rows [0, b)".  Every graph reads the
+ * paged_decode_attention_fp8_store) over rows [0, b)", and one of the step
+ * alone for batches of exactly b.  Every graph reads the
  * same static input buffers and writes the same static outputs, which the
  * CALLER allocates once for max_batch rows and hands to the runner.  A step
  * of B sequences:

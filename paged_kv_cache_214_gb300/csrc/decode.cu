@@ -469,6 +469,13 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   auto empty_bar = [&](int s) { return bars + 8u * (kStagesN + s); };
   const uint32_t stored_bar = bars + 8u * (2 * kStagesN);  // fused store: the new row written
 
+  // The tensor maps are launch parameters, which no earlier kernel writes:
+  // fetch them into the SM's descriptor cache before waiting, so that the
+  // block's first copy does not wait for them.
+  if (threadIdx.x == 0) {
+    tma_prefetch_map(&kmap);
+    tma_prefetch_map(&vmap);
+  }
   // Programmatic dependent launch: the next kernel of the stream may be
   // scheduled once every block of this one has started, and this kernel
   // reads no global memory before the grids it depends on have completed.

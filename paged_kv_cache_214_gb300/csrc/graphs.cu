@@ -6,7 +6,8 @@
 // caller's static buffers, after a one-block kernel that marks the rows past
 // the step's batch as empty.  The batch size reaches that kernel as a launch
 // argument, rewritten in the instantiated graph before a replay whose batch
-// differs from the previous replay's.
+// differs from the previous replay's.  A batch that fills its bucket replays a
+// second graph of the step alone.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -36,6 +37,8 @@ struct Bucket {
   int size = 0;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
+  cudaGraph_t full_graph = nullptr;      // the step alone, for B == size
+  cudaGraphExec_t full_exec = nullptr;
   cudaGraphNode_t pad = nullptr;   // the pad kernel's node in `graph`
   void* pad_func = nullptr;        // that node's kernel, as the node reports it
   int pad_from = 0;                // its current `from` argument
@@ -98,6 +101,8 @@ void release(pkv_decode_graphs* r) {
   for (Bucket& b : r->buckets) {
     if (b.exec) cudaGraphExecDestroy(b.exec);
     if (b.graph) cudaGraphDestroy(b.graph);
+    if (b.full_exec) cudaGraphExecDestroy(b.full_exec);
+    if (b.full_graph) cudaGraphDestroy(b.full_graph);
   }
   if (r->stream) cudaStreamDestroy(r->stream);
   delete r;
@@ -244,6 +249,19 @@ extern "C" int pkv_decode_graphs_create(const pkv_decode_graphs_config* config,
       bk.exec = nullptr;
       return fail(PKV_ERR_LAUNCH);
     }
+    // a batch that fills the bucket needs no padding: the step alone
+    if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+      return fail(PKV_ERR_LAUNCH);
+    rc = step(c, bk.size, s);
+    cudaGraph_t full = nullptr;
+    const cudaError_t end_full = cudaStreamEndCapture(s, &full);
+    bk.full_graph = full;
+    if (rc != PKV_OK) return fail(rc);
+    if (end_full != cudaSuccess || !full) return fail(PKV_ERR_LAUNCH);
+    if (cudaGraphInstantiate(&bk.full_exec, full, 0) != cudaSuccess) {
+      bk.full_exec = nullptr;
+      return fail(PKV_ERR_LAUNCH);
+    }
   }
   if (cudaStreamSynchronize(s) != cudaSuccess) return fail(PKV_ERR_LAUNCH);
   *runner = r;
@@ -268,6 +286,7 @@ extern "C" int pkv_decode_graphs_run(pkv_decode_graphs* runner, int B, pkv_strea
   if (size == 0) return step(runner->cfg, B, s);   // above the largest bucket: eager
   Bucket& bk = *std::find_if(runner->buckets.begin(), runner->buckets.end(),
                              [&](const Bucket& b) { return b.size == size; });
+  if (B == bk.size) return cudaGraphLaunch(bk.full_exec, s) == cudaSuccess ? PKV_OK : PKV_ERR_LAUNCH;
   if (bk.pad_from != B) {
     // the replays already queued keep their own arguments
     cudaKernelNodeParams kp;
