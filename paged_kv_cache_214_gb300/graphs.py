@@ -142,11 +142,12 @@ class DecodeGraphs:
         cfg.workspace = self.workspace.data_ptr()
         cfg.workspace_bytes = self.workspace.numel()
         # the runner's private stream is not ordered after torch's: finish the
-        # fills above first
+        # fills above first; the graphs belong to the pool's device
         torch.cuda.current_stream(dev).synchronize()
         handle = ctypes.c_void_p()
-        pkv._check(lib.pkv_decode_graphs_create(ctypes.byref(cfg), ctypes.byref(handle)),
-                   "pkv_decode_graphs_create")
+        with torch.cuda.device(dev):
+            st = lib.pkv_decode_graphs_create(ctypes.byref(cfg), ctypes.byref(handle))
+        pkv._check(st, "pkv_decode_graphs_create")
         self._h = handle
         n = lib.pkv_decode_graphs_buckets(self._h, None, 0)
         arr = (ctypes.c_int32 * max(n, 1))()
@@ -158,9 +159,12 @@ class DecodeGraphs:
         return pick_bucket(self.buckets, B)
 
     def run(self, B: int, stream=None) -> None:
-        """One step over rows [0, B) of the static buffers."""
+        """One step over rows [0, B) of the static buffers, on `stream` (default:
+        the current stream of the pool's device)."""
         if self._h is None:
             raise RuntimeError("DecodeGraphs has been closed")
+        if stream is None:
+            stream = torch.cuda.current_stream(self.q.device)
         pkv._check(_lib().pkv_decode_graphs_run(self._h, int(B), pkv._stream(stream)),
                    "pkv_decode_graphs_run")
 
@@ -176,7 +180,7 @@ class DecodeGraphs:
         W = self.block_tables.shape[1]
         if block_tables.shape[0] != B or block_tables.shape[1] > W:
             raise ValueError("block_tables must be [B, <= max_blocks_per_seq]")
-        s = torch.cuda.current_stream() if stream is None else stream
+        s = torch.cuda.current_stream(self.q.device) if stream is None else stream
         with torch.cuda.stream(s):
             self.q[:B].copy_(q)
             self.k_new[:B].copy_(k_new)
