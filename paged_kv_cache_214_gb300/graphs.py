@@ -137,7 +137,8 @@ class DecodeGraphs:
                       block_tables=self.block_tables.data_ptr(),
                       context_lens=self.context_lens.data_ptr(), out=self.out.data_ptr(),
                       lse=0 if self.lse is None else self.lse.data_ptr())
-        need = lib.pkv_decode_graphs_workspace_bytes(ctypes.byref(cfg))
+        with torch.cuda.device(dev):   # the split plan reads this device's SM count
+            need = lib.pkv_decode_graphs_workspace_bytes(ctypes.byref(cfg))
         self.workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
         cfg.workspace = self.workspace.data_ptr()
         cfg.workspace_bytes = self.workspace.numel()
