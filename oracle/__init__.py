@@ -21,7 +21,8 @@ Every function cites the passage of the source pages it follows:
 * e4m3_table / quantize_e4m3 / store_fp8 / decode_fp8 — an FP8 (OCP E4M3)
   KV cache with one scale per tensor; the pages only name quantized KV
   transfers ("Why Understand Inference Engine Architecture?", Tensor
-  Parallelism Optimization), so the format is this build's reading.
+  Parallelism Optimization), so the format is a reading of that line: OCP
+  E4M3, nearest code with ties to even, saturated at 448.
 
 bf16 tensors are passed as uint16 bit patterns; outputs are float64.
 """
