@@ -638,6 +638,29 @@ def run_extras(pkv, dev, hbm_peak, args):
             per = a.elapsed_time(b) / 640
             entry["graph_replay_us_per_call"] = round(per * 1e3, 2)
             entry["graph_replay_GB/s"] = round(decode_bytes(w) / (per / 1e3) / 1e9, 1)
+            # the same with PKV_DECODE_METADATA_READY: tables and lengths are
+            # written before the graph and never by a kernel in it
+            g2 = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(s2):
+                call_m = lambda: pkv.paged_decode_attention(  # noqa: E731
+                    q, kc, vc, tables, lens, w.scale, out=out, lse=lse, workspace=ws, stream=s2,
+                    metadata_ready=True)
+                call_m()
+                torch.cuda.synchronize()
+                with torch.cuda.graph(g2, stream=s2):
+                    for _ in range(64):
+                        call_m()
+            stream.wait_stream(s2)
+            g2.replay()
+            torch.cuda.synchronize()
+            a.record(stream)
+            for _ in range(10):
+                g2.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            assert pkv.get_device_error() == pkv.PKV_OK
+            per_m = a.elapsed_time(b) / 640
+            entry["graph_replay_metadata_ready_us_per_call"] = round(per_m * 1e3, 2)
             # the bucketed graph runner: one graph launch (pad, fused store +
             # decode) per call from the host, 64 calls back to back
             from paged_kv_cache_214_gb300 import graphs

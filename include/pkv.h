@@ -12,6 +12,8 @@
  *                            block_tables
  *
  * and, built on them:
+ *   paged_decode_attention_flags      the decode with option bits (tables and
+ *                                     lengths ready before the previous kernel)
  *   paged_decode_attention_store      a decode step's store and decode in one
  *                                     launch
  *   paged_decode_attention_shared_prefix  decode with a prefix that every
@@ -163,6 +165,24 @@ int paged_decode_attention(void* out, float* lse, const void* q,
                            int D, int block_size, int64_t num_blocks, float scale,
                            void* workspace, size_t workspace_bytes,
                            int num_splits, pkv_stream_t stream);
+
+/* paged_decode_attention_flags — paged_decode_attention with option bits.
+ * PKV_DECODE_METADATA_READY: the caller states that block_tables and
+ * context_lens were written before the previous kernel on `stream` started,
+ * and that no kernel still running writes them (for example they came from
+ * host copies at the start of the step, and the previous kernel produced q).
+ * The decode's blocks may then read them while that kernel finishes, before
+ * they wait for it; everything else (q, the pools, out, lse, the workspace)
+ * is still touched only after the wait.  Results are bit-identical to
+ * paged_decode_attention; if the statement is false they are undefined.
+ * Other bits: PKV_ERR_ARG.  Everything else as paged_decode_attention. */
+#define PKV_DECODE_METADATA_READY 1u
+int paged_decode_attention_flags(void* out, float* lse, const void* q, const void* k_cache,
+                                 const void* v_cache, const int32_t* block_tables,
+                                 int max_blocks_per_seq, const int32_t* context_lens, int B,
+                                 int Hq, int Hkv, int D, int block_size, int64_t num_blocks,
+                                 float scale, void* workspace, size_t workspace_bytes,
+                                 int num_splits, unsigned flags, pkv_stream_t stream);
 
 /* paged_decode_attention_store — kv_cache_store of the step's new tokens and
  * paged_decode_attention over the updated cache in one launch, the way the

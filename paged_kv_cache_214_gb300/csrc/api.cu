@@ -286,6 +286,21 @@ extern "C" int paged_decode_attention(void* out, float* lse, const void* q, cons
   return decode_entry(a, D, block_size, nullptr, stream);
 }
 
+extern "C" int paged_decode_attention_flags(void* out, float* lse, const void* q,
+                                            const void* k_cache, const void* v_cache,
+                                            const int32_t* block_tables, int max_blocks_per_seq,
+                                            const int32_t* context_lens, int B, int Hq, int Hkv,
+                                            int D, int block_size, int64_t num_blocks,
+                                            float scale, void* workspace,
+                                            size_t workspace_bytes, int num_splits,
+                                            unsigned flags, pkv_stream_t stream) {
+  if (flags & ~static_cast<unsigned>(PKV_DECODE_METADATA_READY)) return PKV_ERR_ARG;
+  DecodeArgs a{out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+               B, Hq, Hkv, num_blocks, scale, workspace, workspace_bytes, num_splits, 0};
+  a.metadata_ready = (flags & PKV_DECODE_METADATA_READY) ? 1 : 0;
+  return decode_entry(a, D, block_size, nullptr, stream);
+}
+
 extern "C" int paged_decode_attention_store(
     void* out, float* lse, const void* q, const void* k_new, const void* v_new,
     int64_t k_tok_stride, int64_t v_tok_stride, const int32_t* slot_mapping, void* k_cache,

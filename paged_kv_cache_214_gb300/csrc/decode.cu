@@ -89,6 +89,7 @@ struct DecodeParams {
   // (sequence, query head); this kernel then covers [prefix_tokens, ctx) only
   // and folds that partial into its merge.
   int prefix_tokens;
+  int metadata_ready;       // tables and lengths may be read before the dependency wait
   int prefix_splits;        // partials per row of the shared-prefix pass
   const float* prefix_o;    // [B*Hq, prefix_splits, 128]
   const float* prefix_lse;  // [B*Hq, prefix_splits] log2-sum-exp
@@ -478,9 +479,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   }
   // Programmatic dependent launch: the next kernel of the stream may be
   // scheduled once every block of this one has started, and this kernel
-  // reads no global memory before the grids it depends on have completed.
+  // reads no global memory before the grids it depends on have completed
+  // (with metadata_ready: none but block_tables and context_lens, which the
+  // caller wrote before those grids; the wait then follows the block's
+  // early exit below, before anything else is read or written).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (!p.metadata_ready) asm volatile("griddepcontrol.wait;" ::: "memory");
   const int split = blockIdx.x;
   const int hg = blockIdx.y;  // kv head * head_groups + query head group
   const int b = blockIdx.z;
@@ -527,6 +531,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap kmap,
   };
   const int nsplit = (ctx - P + split_tokens - 1) / split_tokens;
   if (split >= (nsplit > 0 ? nsplit : 1)) return;  // whole block exits: no work
+  if (p.metadata_ready) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // Fused store: the blocks of a sequence's last range write the step's new
   // token (see below); a sequence with no token to attend takes none.
@@ -1035,6 +1040,7 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& plan, unsigned* err,
   prm.num_blocks = a.num_blocks;
   prm.scale_log2 = a.scale * 1.4426950408889634f;
   prm.prefix_tokens = a.prefix_tokens;
+  prm.metadata_ready = a.metadata_ready;
   prm.prefix_splits = plan.prefix_splits;
   prm.new_slots = a.new_slots;
   prm.k_new = static_cast<const __nv_bfloat16*>(a.k_new);

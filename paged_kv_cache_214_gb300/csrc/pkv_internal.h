@@ -79,6 +79,10 @@ struct DecodeArgs {
   const void* k_new = nullptr;
   const void* v_new = nullptr;
   int64_t k_new_stride = 0, v_new_stride = 0;
+  // block_tables and context_lens were written before the stream's previous
+  // kernel (PKV_DECODE_METADATA_READY): blocks may read them before waiting
+  // for that kernel
+  int metadata_ready = 0;
 };
 
 // Argument checks of a single-query decode call (pointers, alignment, pool

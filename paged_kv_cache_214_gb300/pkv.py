@@ -26,6 +26,7 @@ PKV_ERR_WORKSPACE = -3
 PKV_ERR_LAUNCH = -4
 PKV_ERR_DEVICE_INDEX = -5
 PKV_ERR_TIMEOUT = -6
+PKV_DECODE_METADATA_READY = 1
 
 _lock = threading.Lock()
 _lib = None
@@ -62,6 +63,10 @@ def load_library(path: str = LIB_PATH):
         lib.paged_decode_attention.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32,
                                                i32, i64, f32, P, sz, i32, P]
         lib.paged_decode_attention.restype = i32
+        lib.paged_decode_attention_flags.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32,
+                                                     i32, i32, i64, f32, P, sz, i32,
+                                                     ctypes.c_uint32, P]
+        lib.paged_decode_attention_flags.restype = i32
         lib.paged_decode_shared_prefix_workspace_bytes.argtypes = [i32] * 8
         lib.paged_decode_shared_prefix_workspace_bytes.restype = sz
         lib.paged_decode_attention_shared_prefix.argtypes = [P, P, P, P, P, P, i32, P, i32, i32,
@@ -215,10 +220,13 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
                            scale: float, out: Optional[torch.Tensor] = None,
                            lse: Optional[torch.Tensor] = None,
                            workspace: Optional[torch.Tensor] = None, num_splits: int = 0,
-                           want_lse: bool = True, stream=None
+                           want_lse: bool = True, stream=None, metadata_ready: bool = False
                            ) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """q bf16 [B, Hq, D]; block_tables int32 [B, max_blocks]; context_lens int32
-    [B].  Returns (out bf16 [B, Hq, D], lse fp32 [B, Hq] or None)."""
+    [B].  Returns (out bf16 [B, Hq, D], lse fp32 [B, Hq] or None).
+    metadata_ready: block_tables and context_lens were written before the
+    stream's previous kernel started and no running kernel writes them
+    (PKV_DECODE_METADATA_READY of paged_decode_attention_flags)."""
     lib = load_library()
     NB, bs, Hkv, D = _pool_dims(k_cache, v_cache)
     _need(q, "q", torch.bfloat16, 3)
@@ -241,6 +249,13 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     if workspace is None and need:
         workspace = decode_workspace(need, q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if metadata_ready:
+        _check(lib.paged_decode_attention_flags(
+            _ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+            maxblk, _ptr(context_lens), B, Hq, Hkv, D, bs, NB, float(scale), _ptr(workspace),
+            ws_bytes, int(num_splits), PKV_DECODE_METADATA_READY, _stream(stream)),
+            "paged_decode_attention_flags")
+        return out, lse
     _check(lib.paged_decode_attention(_ptr(out), _ptr(lse), _ptr(q), _ptr(k_cache),
                                       _ptr(v_cache), _ptr(block_tables), maxblk,
                                       _ptr(context_lens), B, Hq, Hkv, D, bs, NB, float(scale),

@@ -166,6 +166,14 @@ def test_workspace_query_and_split_plan(lib):
         pkv.paged_decode_num_splits(8, 32, 8, 64, 512, 256, 0)
 
 
+def test_decode_flags_reject_unknown_bits(lib):
+    # refused on the host, before anything is read or launched
+    st = lib.paged_decode_attention_flags(None, None, None, None, None, None, 1, None, 1, 8, 8,
+                                          128, 256, 1, 0.1, None, 0, 0, 2, None)
+    assert st == pkv.PKV_ERR_ARG
+    assert pkv.PKV_DECODE_METADATA_READY == 1
+
+
 def test_status_strings(lib):
     for code in range(-6, 1):
         assert pkv.status_string(code).startswith("PKV_")

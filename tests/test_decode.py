@@ -95,6 +95,60 @@ def test_small_batch_short_contexts_one_split(Hq, Hkv):
     run_and_check(w, what=f"one split Hq={Hq},Hkv={Hkv}")
 
 
+@pytest.mark.parametrize("lens,Hq,Hkv", [([17, 256, 300, 513], 16, 8),
+                                          ([3000, 900, 5000, 257, 64, 1], 32, 8)])
+def test_metadata_ready_flag(lens, Hq, Hkv):
+    """PKV_DECODE_METADATA_READY (tables and lengths read before the wait for
+    the previous kernel): the one-split two-group form and a split batch match
+    the oracle and equal the plain call bit for bit, also as two calls in a
+    replayed CUDA graph whose inputs change between replays."""
+    dev = "cuda"
+    w = W.make_decode(lens, Hq, Hkv, 64, 3600 + Hq, store_new_token=False)
+    q, kc, vc = w.q.to(dev), w.k_cache.to(dev), w.v_cache.to(dev)
+    tables, ctx = w.block_tables.to(dev), w.context_lens.to(dev)
+    o1, l1 = pkv.paged_decode_attention(q, kc, vc, tables, ctx, w.scale)
+    torch.cuda.synchronize()
+    o2, l2 = pkv.paged_decode_attention(q, kc, vc, tables, ctx, w.scale, metadata_ready=True)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == pkv.PKV_OK
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    ref_o, ref_l = oracle.decode(bits(w.q), bits(w.k_cache), bits(w.v_cache),
+                                 w.block_tables.numpy(), w.context_lens.numpy(), w.scale)
+    assert_close(o2, l2, ref_o, ref_l, "metadata ready")
+
+    # two flagged calls in one graph; tables and lengths rewritten between
+    # replays by host copies, finished before the replay starts
+    w2 = W.make_decode([max(1, L // 2) for L in lens], Hq, Hkv, 64, 3700 + Hq,
+                       store_new_token=False, max_blocks_per_seq=w.block_tables.shape[1])
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, Hq), dtype=torch.float32, device=dev)
+    need = pkv.paged_decode_workspace_bytes(w.B, Hq, Hkv, 128, tables.shape[1])
+    ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    call = lambda: pkv.paged_decode_attention(q, kc, vc, tables, ctx, w.scale, out=out,  # noqa: E731
+                                              lse=lse, workspace=ws, stream=s,
+                                              metadata_ready=True)
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+        call()
+    for ww in (w2, w):
+        tables.copy_(ww.block_tables)
+        ctx.copy_(ww.context_lens)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == pkv.PKV_OK
+        ref_o, ref_l = oracle.decode(bits(w.q), bits(w.k_cache), bits(w.v_cache),
+                                     ww.block_tables.numpy(), ww.context_lens.numpy(), w.scale)
+        assert_close(out, lse, ref_o, ref_l, "metadata ready in a graph")
+
+
 def test_empty_context_gives_zero_and_neg_inf():
     w = W.make_decode([0, 300, 0], 16, 8, 8, 3100, store_new_token=False)
     dev = "cuda"
